@@ -1,0 +1,81 @@
+/*
+ * Plain CPU oracle for the EntroPack codec.  TEST INFRASTRUCTURE ONLY:
+ * only the tests, the smoke check and the benchmark's CPU-baseline leg may
+ * load it.  It shares no code, header or table with the CUDA library.
+ *
+ * Method passages followed ("EntroPack: Fast and Accurate Entropy-Coded
+ * Weight Compression at Arbitrary Bitrates", Abstract):
+ *   row-normalised E8 lattice quantisation        -> oracle_row_rms, oracle_e8_nearest
+ *   conditional probability model of coordinates  -> oracle_block_symbols
+ *   sampled storage estimates select resolution   -> oracle_estimate_bpp, oracle_select_j
+ *   entropy coding in independently decodable tiles -> oracle_rans_*, oracle_encode
+ *   fused decode + reconstruction into BF16/FP16/FP8/INT8 -> oracle_decode
+ * Lossless tiled ANS ("EntroPack PyTorch Guide", section "Choose a
+ * compression contract", TileANSConfig) -> oracle_encode_lossless.
+ * The stream layout and every constant are the readings written down in
+ * FORMAT.md of this repository.
+ *
+ * Parity pins (tests/test_oracle_*.py): brute-force E8 search, the E8
+ * second moment 929/12960, rANS round trip and code-length bounds,
+ * conversions against torch, the Gaussian rate-distortion closed form,
+ * bitwise lossless recovery.  Parity unpinned: the exact resolution index
+ * chosen by the rate search (only its determinism and its distance to the
+ * target are pinned).
+ */
+#ifndef ENTROPACK_ORACLE_H
+#define ENTROPACK_ORACLE_H
+#include <stddef.h>
+#include <stdint.h>
+
+/* nearest point of E8 to x; writes the integer coordinates a[8] and the coset */
+void oracle_e8_nearest(const double x[8], int64_t a[8], int *coset);
+
+double oracle_row_rms(const uint16_t *w_row, int64_t K);
+double oracle_delta(int j);
+double oracle_rn7(double v);
+double oracle_tr7(double v);
+
+/* 12-bit normaliser of 256 counts */
+void oracle_normalize(const uint64_t counts[256], uint32_t freq[256]);
+
+/* rANS on one lane: syms/ freqs given; words written in decode order */
+int oracle_rans_encode(const uint8_t *syms, const uint8_t *ctx, int64_t n, const uint32_t *freq_by_ctx,
+                       uint32_t *state, uint16_t *words, int64_t max_words, int64_t *n_words);
+int oracle_rans_decode(const uint16_t *words, int64_t n_words, uint32_t state, const uint8_t *ctx, int64_t n,
+                       const uint32_t *freq_by_ctx, uint8_t *syms_out);
+
+/* conversions from the format definitions */
+uint16_t oracle_f32_to_bf16(float v);
+uint16_t oracle_f32_to_f16(float v);
+uint8_t oracle_f32_to_e4m3_satfinite(float v);
+int8_t oracle_f32_to_int8(float v);
+double oracle_bf16_to_f64(uint16_t b);
+
+/* symbols of one quantised block (returns the escape count, fills bytes/payloads) */
+int oracle_block_symbols(const int64_t a[8], int coset, uint8_t u[8], uint8_t ctx[8], int32_t payload[8]);
+
+/* rate estimate (bits per parameter) on sampled rows at index j */
+double oracle_estimate_bpp(const uint16_t *w, int64_t M, int64_t K, float sample_frac, int j);
+int oracle_select_j(const uint16_t *w, int64_t M, int64_t K, float target_bpp, float sample_frac, int *j_lo_out);
+
+/* full encoders; *blob is malloc'ed, free with oracle_free */
+int oracle_encode(const uint16_t *w, int64_t M, int64_t K, float target_bpp, int container, float sample_frac,
+                  uint8_t **blob, size_t *bytes);
+int oracle_encode_lossless(const uint16_t *w, int64_t M, int64_t K, uint8_t **blob, size_t *bytes);
+void oracle_free(void *p);
+
+/* decode tiles [t_lo, t_hi) into out (M*K elements of the container) and,
+ * for FP8/INT8, the output row scales t_r (written for all rows when t_lo == 0) */
+int oracle_decode(const uint8_t *blob, size_t bytes, void *out, float *row_scale_out, int64_t t_lo, int64_t t_hi);
+/* the symbol byte u coded for every coordinate (M*K bytes, matrix order) */
+int oracle_decode_symbols(const uint8_t *blob, size_t bytes, uint8_t *sym_out, int64_t t_lo, int64_t t_hi);
+
+/* the lattice point of every coordinate as k = 2q (M*K int32, matrix order; lossy blobs) */
+int oracle_decode_lattice(const uint8_t *blob, size_t bytes, int32_t *k_out, int64_t t_lo, int64_t t_hi);
+/* batch conversions used by the conversion pins: kind 0 bf16, 1 fp16, 2 e4m3 satfinite, 3 int8 */
+void oracle_convert_f32(int kind, int64_t n, const float *in, void *out);
+
+/* fp64 reference GEMM: y[t, n] = sum_k x[t, k] * w[n, k] for rows t of x */
+void oracle_gemm_f64(const double *x, const double *w, double *y, int64_t T, int64_t N, int64_t K);
+
+#endif

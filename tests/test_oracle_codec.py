@@ -1,0 +1,186 @@
+"""Pins of the oracle's whole lossy codec (FORMAT.md §4).
+
+* every decoded lattice point equals the plain nearest-E8 quantisation of
+  w / g_r done here block by block (checks symbols, contexts, escapes,
+  tables and rANS end to end against the quantiser);
+* high-resolution rate-distortion of E8 on Gaussian rows:
+  rel-L2 ~ sqrt(2 pi e G(E8)) 2^-R and est(Delta) ~ h(N(0,1)) - log2 Delta;
+* actual_bpp >= empirical entropy of the coded symbols + metadata, and
+  actual_bpp > target_bpp (the pages report actual above target);
+* rate search lands within one grid step of the target.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+G_E8 = 929.0 / 12960.0
+H_NORMAL = 0.5 * math.log2(2 * math.pi * math.e)  # 2.047 bits
+
+
+def _w(seed=1, M=256, K=1024, std=0.02):
+    return synth.normal_bf16(seed, M, K, std=std)
+
+
+def _row_steps(blob):
+    h = oracle.header(blob)
+    return np.frombuffer(blob, dtype=np.float32, count=h["M"], offset=h["rowmeta_off"]).astype(np.float64)
+
+
+@pytest.mark.parametrize("target", [2.5, 4.0])
+def test_lattice_points_equal_direct_quantisation(target):
+    w = synth.rows_outliers_bf16(2, 64, 256)
+    blob = oracle.encode(w, target)
+    k = oracle.decode_lattice(blob)
+    g = _row_steps(blob)
+    W = synth.bf16_to_f32(w).astype(np.float64)
+    for r in range(w.shape[0]):
+        for c0 in range(0, w.shape[1], 8):
+            if g[r] == 0:
+                want = np.zeros(8)
+            else:
+                a, c = oracle.e8_nearest(W[r, c0:c0 + 8] / g[r])
+                want = 2 * a + c
+            assert (k[r, c0:c0 + 8] == want).all(), (r, c0)
+    # E8 membership of every decoded block: common parity, even integer-part sum
+    kb = k.reshape(-1, 8)
+    assert ((kb & 1) == (kb[:, :1] & 1)).all()
+    assert (((kb - (kb[:, :1] & 1)) // 2).sum(axis=1) % 2 == 0).all()
+
+
+def test_escapes_round_trip():
+    # heavy outliers at a high rate force escape payloads in every context
+    w = synth.rows_outliers_bf16(3, 32, 128, frac=0.05, k_sigma=40.0)
+    blob = oracle.encode(w, 6.0)
+    sym = oracle.decode_symbols(blob)
+    assert (sym[:, ::8] <= 1).any() and (sym[:, 1::8] == 0).any()
+    k = oracle.decode_lattice(blob)
+    assert np.abs(k).max() > 127
+    g = _row_steps(blob)
+    W = synth.bf16_to_f32(w).astype(np.float64)
+    for r in range(32):
+        for c0 in range(0, 128, 8):
+            a, c = oracle.e8_nearest(W[r, c0:c0 + 8] / g[r])
+            assert (k[r, c0:c0 + 8] == 2 * a + c).all()
+
+
+@pytest.mark.parametrize("target", [3.0, 3.5, 4.0, 4.5])
+def test_gaussian_rate_distortion(target):
+    w = _w(11, 256, 1024)
+    blob = oracle.encode(w, target)
+    y, _ = oracle.decode(blob)
+    W = synth.bf16_to_f32(w).astype(np.float64)
+    rel = np.linalg.norm(oracle.container_to_f64(y, "bf16") - W) / np.linalg.norm(W)
+    h = oracle.header(blob)
+    est = oracle.estimate_bpp(w, 1.0, h["j"])
+    theory = math.sqrt(2 * math.pi * math.e * G_E8) * 2.0 ** (-est)
+    assert abs(rel / theory - 1) < 0.10, (rel, theory, est)
+
+
+@pytest.mark.parametrize("j", [-200, -150, -100])
+def test_estimate_follows_differential_entropy(j):
+    w = _w(12, 256, 1024)
+    est = oracle.estimate_bpp(w, 1.0, j)
+    assert abs(est - (H_NORMAL - j / 64.0)) < 0.03, est
+
+
+def _empirical_entropy_bits(sym):
+    blocks = sym.reshape(-1, 8).astype(np.int64)
+    c = blocks[:, 0] & 1
+    total, n_esc = 0.0, 0
+    groups = {0: blocks[:, 0]}
+    for cc in (0, 1):
+        groups[1 + cc] = blocks[c == cc, 1:7].ravel()
+        groups[3 + cc] = blocks[c == cc, 7]
+    for ctx, vals in groups.items():
+        if vals.size == 0:
+            continue
+        cnt = np.bincount(vals, minlength=256).astype(np.float64)
+        nz = cnt[cnt > 0]
+        total += float((nz * np.log2(vals.size / nz)).sum())
+    n_esc = int((blocks[:, 0] <= 1).sum() + (blocks[:, 1:] == 0).sum())
+    return total + 16 * n_esc
+
+
+def test_actual_bpp_bounds():
+    w = _w(1, 256, 1024)
+    blob = oracle.encode(w, 4.0)
+    h = oracle.header(blob)
+    actual = 8 * len(blob) / w.size
+    sym = oracle.decode_symbols(blob)
+    meta_bytes = h["payload_off"] + h["n_tiles"] * 24
+    bound = _empirical_entropy_bits(sym) + 8 * meta_bytes
+    assert 8 * len(blob) >= bound * (1 - 1e-3)
+    assert actual > h["target_bpp"]
+    assert actual < h["target_bpp"] + 0.25
+
+
+def test_rate_search_is_locally_best():
+    w = synth.rows_outliers_bf16(2, 256, 512)
+    for target in (2.5, 3.5, 4.5):
+        j, jlo = oracle.select_j(w, target, 0.05)
+        e = {d: oracle.estimate_bpp(w, 0.05, j + d) for d in (-1, 0, 1)}
+        assert e[-1] >= e[0] >= e[1]
+        assert abs(e[0] - target) <= min(abs(e[-1] - target), abs(e[1] - target)) + 1e-12
+        assert abs(e[0] - target) < 1.0 / 64 + 0.02
+        assert oracle.select_j(w, target, 0.05) == (j, jlo)
+
+
+def test_zero_rows_and_constant_rows():
+    w = _w(4, 64, 256)
+    w[3] = 0
+    w[10] = 0x8000  # -0
+    w[20] = 0x3C4A
+    blob = oracle.encode(w, 4.0)
+    y, _ = oracle.decode(blob)
+    assert (y[3] == 0).all() and (y[10] == 0).all()
+    W = synth.bf16_to_f32(w).astype(np.float64)
+    rel = np.abs(oracle.container_to_f64(y[20:21], "bf16") - W[20:21]).max() / abs(W[20, 0])
+    assert rel < 0.1
+
+
+@pytest.mark.parametrize("container", ["fp16", "fp8", "int8"])
+def test_containers_scales(container):
+    w = _w(5, 64, 256)
+    blob = oracle.encode(w, 3.0, container)
+    y, rs = oracle.decode(blob)
+    W = synth.bf16_to_f32(w).astype(np.float64)
+    Wh = oracle.container_to_f64(y, container, rs)
+    rel = np.linalg.norm(Wh - W) / np.linalg.norm(W)
+    ref = np.linalg.norm(oracle.container_to_f64(oracle.decode(oracle.encode(w, 3.0))[0], "bf16") - W) / np.linalg.norm(W)
+    # FP16 adds nothing; FP8 (3 mantissa bits) and INT8 add their own rounding on top of the lattice error
+    limit = {"fp16": 1.01, "fp8": 1.6, "int8": 1.3}[container]
+    assert rel <= ref * limit, (rel, ref)
+    if container == "int8":
+        assert np.abs(y.astype(np.int64)).max() <= 127
+    if container == "fp8":
+        assert rs is not None and (rs > 0).all()
+
+
+def test_rejects_bad_inputs():
+    w = _w(6, 64, 256)
+    bad = w.copy()
+    bad[5, 7] = 0x7FC0
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.encode(bad)
+    assert e.value.name == "nonfinite"
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.encode(w[:48])
+    assert e.value.name == "shape"
+
+
+def test_corrupt_blob_is_reported():
+    w = _w(7, 64, 256)
+    blob = bytearray(oracle.encode(w, 4.0))
+    h = oracle.header(bytes(blob))
+    for pos in (h["payload_off"] + 40, h["payload_off"] + 300, len(blob) - 20):
+        b2 = bytearray(blob)
+        b2[pos] ^= 0x5A
+        with pytest.raises(oracle.OracleError) as e:
+            oracle.decode(bytes(b2))
+        assert e.value.name == "corrupt"
+    with pytest.raises(oracle.OracleError):
+        oracle.decode(bytes(blob[:-16]))
