@@ -1,0 +1,639 @@
+// GPU decode of EntroPack streams on B300 (sm_103a): fused rANS symbol
+// decoding, E8 reconstruction, row rescaling and container conversion
+// ("EntroPack: Fast and Accurate Entropy-Coded Weight Compression at Arbitrary
+// Bitrates", Abstract: "fast, fused symbol decoding and numerical weight
+// reconstruction on the GPU"; containers BF16, FP16, FP8, INT8).
+//
+// Work decomposition.  A tile (32 x 128 weights) carries 4 independent rANS
+// lanes; one thread owns one lane, so one warp decodes 8 tiles.  Every CTA
+// first expands the stream's 12-bit frequency tables into 4096-entry slot
+// tables in shared memory (one u32 per slot: symbol byte | f | slot - cum),
+// then its warps walk tile groups.  A lane decodes its 128 blocks of 8
+// coordinates in the format's order; lanes 2h and 2h+1 of a tile write the two
+// halves of one 32-byte row segment, so each warp-wide 128-bit store covers
+// whole sectors.  Escapes (values beyond the direct byte range) are rare: the
+// fast path is branch-free and a warp-uniform test sends a block with any
+// escape through the slow path.
+//
+// Reconstruction uses the format's 7-bit row steps: the symbol byte u = 2q+128
+// is spliced into the float 0x4AC00000 + u (= 6291520 + q) and one FMA with
+// c = -g * 6291520 (exact) yields fp32(g * q) with a single rounding.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "ep_format.hpp"
+
+namespace ep {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarpsPerCta = kThreads / 32;
+constexpr int kTilesPerWarp = 8;
+constexpr int kSlots = 4096;
+constexpr uint32_t kMagicF = 0x4AC00000u;  // float 6291456 = 1.5 * 2^22 (spacing 0.5)
+constexpr float kMagicQ = 6291520.0f;       // 6291456 + 128 / 2
+
+enum Kind { K_BF16 = 0, K_FP16 = 1, K_FP8 = 2, K_INT8 = 3, K_LOSSLESS = 4 };
+
+struct DecodeArgs {
+    const uint8_t* blob;
+    const uint64_t* tile_off;
+    const uint8_t* payload;
+    uint64_t payload_bytes;
+    const float* g;  // row steps
+    const float* m;  // FP8/INT8 multipliers
+    const float* t;  // FP8/INT8 output scales
+    uint32_t ctx_off[8];
+    int n_ctx;
+    void* out;
+    float* scale_out;
+    uint8_t* sym_out;
+    uint32_t* status;
+    int64_t rows, cols, n_tiles;
+    int64_t tiles_per_row;
+};
+
+// ---------------------------------------------------------------- tables
+// Expand (lo, n, f[n]) records into slot tables: entry = u << 24 | f << 12 | (slot - cum).
+__device__ void build_tables(const DecodeArgs& a, uint32_t* tab, uint32_t* fr, uint32_t* cu) {
+    const int n_ctx = a.n_ctx;
+    for (int i = threadIdx.x; i < n_ctx * 256; i += blockDim.x) fr[i] = 0;
+    __syncthreads();
+    for (int c = 0; c < n_ctx; c++) {
+        const uint16_t* rec = reinterpret_cast<const uint16_t*>(a.blob + a.ctx_off[c]);
+        // the host validated these records; a device copy that differs from the
+        // host copy must still not write outside the table (it then fails the
+        // lane end checks)
+        const int lo = rec[0] < 256 ? rec[0] : 256;
+        const int n = rec[1] < 256 - lo ? rec[1] : 256 - lo;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) fr[c * 256 + lo + i] = rec[2 + i] & 0xFFFu;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < n_ctx) {  // exclusive prefix sum of one context per warp
+        uint32_t v[8], s = 0;
+        for (int k = 0; k < 8; k++) {
+            v[k] = fr[warp * 256 + lane * 8 + k];
+            s += v[k];
+        }
+        uint32_t incl = s;
+        for (int d = 1; d < 32; d <<= 1) {
+            uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += o;
+        }
+        uint32_t run = incl - s;
+        for (int k = 0; k < 8; k++) {
+            cu[warp * 256 + lane * 8 + k] = run;
+            run += v[k];
+        }
+    }
+    __syncthreads();
+    // chunks of 32 consecutive slots: binary search the first, then walk
+    for (int ch = threadIdx.x; ch < n_ctx * (kSlots / 32); ch += blockDim.x) {
+        const int c = ch / (kSlots / 32);
+        const uint32_t s0 = (uint32_t)(ch % (kSlots / 32)) * 32u;
+        const uint32_t* C = cu + c * 256;
+        const uint32_t* F = fr + c * 256;
+        int lo = 0, hi = 255;  // largest u with cum[u] <= s0
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (C[mid] <= s0) lo = mid; else hi = mid - 1;
+        }
+        int u = lo;
+        for (uint32_t s = s0; s < s0 + 32u; s++) {
+            while (u < 255 && s >= C[u] + F[u]) u++;
+            tab[c * kSlots + s] = ((uint32_t)u << 24) | (F[u] << 12) | ((s - C[u]) & 0xFFFu);
+        }
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------- rANS lane
+struct Lane {
+    uint32_t x;            // state
+    uint32_t next;         // next renormalisation word (prefetched)
+    const uint16_t* wp;    // position of `next` in the lane's words
+    const uint16_t* wend;  // one past the lane's last word
+    const uint16_t* safe;  // in-bounds address used once the lane is exhausted
+
+    __device__ __forceinline__ void refill() {
+        if (x < kRansL) {
+            x = (x << 16) | next;
+            ++wp;
+            next = __ldg(wp < wend ? wp : safe);
+        }
+    }
+    // one table symbol; returns the slot entry
+    __device__ __forceinline__ uint32_t sym(const uint32_t* tab) {
+        const uint32_t e = tab[x & (kProbScale - 1)];
+        x = ((e >> 12) & 0xFFFu) * (x >> kProbBits) + (e & 0xFFFu);
+        refill();
+        return e;
+    }
+    // one uniform byte (f = 16, cum = 16 * byte)
+    __device__ __forceinline__ uint32_t byte() {
+        const uint32_t slot = x & (kProbScale - 1);
+        x = 16u * (x >> kProbBits) + (slot & 15u);
+        refill();
+        return slot >> 4;
+    }
+};
+
+__device__ __forceinline__ void flag(uint32_t* status, uint32_t bits) { atomicOr(status, bits); }
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, int kind) {
+    if (kind == K_BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack4_fp8(float a, float b, float c, float d) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+__device__ __forceinline__ uint32_t i8(float v) {
+    int i = __float2int_rn(v);
+    i = max(-127, min(127, i));
+    return (uint32_t)i & 0xFFu;
+}
+
+__device__ __forceinline__ uint32_t pack4_i8(float a, float b, float c, float d) {
+    return i8(a) | (i8(b) << 8) | (i8(c) << 16) | (i8(d) << 24);
+}
+
+// ------------------------------------------------------------- one group
+// One warp decodes tile group `grp` (8 tiles, one rANS lane per thread).
+// Returns without touching memory for tiles past the end.
+template <int KIND, bool DUMP>
+__device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t* tab, int64_t grp,
+                                             uint32_t* status) {
+    const int lane = threadIdx.x & 31, l = lane & 3, tig = lane >> 2;
+    const int64_t K = a.cols;
+    constexpr uint32_t kHdr = (KIND == K_LOSSLESS ? kRawBytesPerTile : 0) + kTileHeaderBytes;
+    const uint16_t* safe = reinterpret_cast<const uint16_t*>(a.payload);
+    {
+        const int64_t tile = grp * kTilesPerWarp + tig;
+        bool active = tile < a.n_tiles;
+        uint64_t o0 = 0, o1 = 0;
+        if (active) {
+            o0 = a.tile_off[tile];
+            o1 = a.tile_off[tile + 1];
+            if (o0 > o1 || o1 > a.payload_bytes || (o0 & 15u) || o1 - o0 < kHdr) {
+                if (l == 0) flag(status, EP_STATUS_TILE_BOUNDS);
+                active = false;
+            }
+        }
+        const uint8_t* tb = a.payload + (active ? o0 : 0);
+        const uint8_t* th = tb + (KIND == K_LOSSLESS ? kRawBytesPerTile : 0);
+        Lane ln;
+        ln.x = kRansL;
+        ln.safe = safe;
+        ln.wp = ln.wend = safe;
+        if (active) {
+            const uint2 nwv = *reinterpret_cast<const uint2*>(th + 16);
+            const uint32_t nw[4] = {nwv.x & 0xFFFFu, nwv.x >> 16, nwv.y & 0xFFFFu, nwv.y >> 16};
+            const uint32_t total = nw[0] + nw[1] + nw[2] + nw[3];
+            uint32_t before = 0;
+            for (int i = 0; i < 4; i++) before += (i < l) ? nw[i] : 0u;
+            if (kHdr + 2ull * total > o1 - o0) {
+                if (l == 0) flag(status, EP_STATUS_TILE_BOUNDS);
+                active = false;
+            } else {
+                ln.x = reinterpret_cast<const uint32_t*>(th)[l];
+                ln.wp = reinterpret_cast<const uint16_t*>(th + kTileHeaderBytes) + before;
+                const uint32_t mine = l == 0 ? nw[0] : (l == 1 ? nw[1] : (l == 2 ? nw[2] : nw[3]));
+                ln.wend = ln.wp + mine;
+            }
+        }
+        ln.next = __ldg(ln.wp < ln.wend ? ln.wp : safe);
+
+        const int64_t tr0 = (tile / a.tiles_per_row) * kTileRows;
+        const int64_t tc0 = (tile % a.tiles_per_row) * kTileCols;
+        // element offset of this lane's first block (row 2*0 + l/2, column 8*(l&1))
+        const int64_t base = (tr0 + (l >> 1)) * K + tc0 + 8 * (l & 1);
+        bool esc_bad = false;
+
+        for (int j = 0; j < kBlocksPerLane; j++) {
+            const int m2 = j & 15, slab = j >> 4;
+            const int64_t row = tr0 + 2 * m2 + (l >> 1);
+            const int64_t eoff = base + (int64_t)(2 * m2) * K + 16 * slab;
+            if (KIND == K_LOSSLESS) {
+                uint2 raw = make_uint2(0, 0);
+                if (active) raw = *reinterpret_cast<const uint2*>(tb + 8 * (4 * j + l));
+                uint32_t e[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) e[i] = ln.sym(tab);
+                uint32_t w[4];
+#pragma unroll
+                for (int h = 0; h < 4; h++) {
+                    const uint32_t rw = (h < 2 ? raw.x : raw.y) >> (16 * (h & 1));
+                    const uint32_t r0 = rw & 0xFFu, r1 = (rw >> 8) & 0xFFu;
+                    const uint32_t v0 = ((r0 & 0x80u) << 8) | ((e[2 * h] >> 24) << 7) | (r0 & 0x7Fu);
+                    const uint32_t v1 = ((r1 & 0x80u) << 8) | ((e[2 * h + 1] >> 24) << 7) | (r1 & 0x7Fu);
+                    w[h] = v0 | (v1 << 16);
+                }
+                if (active) {
+                    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + eoff) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                    if (DUMP) {
+                        uint2 s;
+                        s.x = (e[0] >> 24) | ((e[1] >> 24) << 8) | ((e[2] >> 24) << 16) | (e[3] & 0xFF000000u);
+                        s.y = (e[4] >> 24) | ((e[5] >> 24) << 8) | ((e[6] >> 24) << 16) | (e[7] & 0xFF000000u);
+                        *reinterpret_cast<uint2*>(a.sym_out + eoff) = s;
+                    }
+                }
+                continue;
+            }
+            const float g = active ? __ldg(a.g + row) : 0.f;
+            float mult = g;
+            if (KIND == K_FP8 || KIND == K_INT8) mult = active ? __ldg(a.m + row) : 0.f;
+            uint32_t e[8];
+            e[0] = ln.sym(tab);
+            const uint32_t c = (e[0] >> 24) & 1u;
+            const uint32_t* t1 = tab + (1u + c) * kSlots;
+#pragma unroll
+            for (int i = 1; i < 7; i++) e[i] = ln.sym(t1);
+            e[7] = ln.sym(tab + (3u + c) * kSlots);
+            const uint32_t u7 = e[7] >> 24;  // coded byte, before the parity increment
+            bool esc = e[0] < (2u << 24);
+#pragma unroll
+            for (int i = 1; i < 8; i++) esc |= e[i] < (1u << 24);
+            esc = esc && active;
+            uint32_t F[8];
+            if (__any_sync(0xffffffffu, esc)) {
+                int32_t B[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) B[i] = (int32_t)(e[i] >> 24);
+                if (esc) {
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        const bool is_esc = (i == 0) ? (B[0] <= 1) : (B[i] == 0);
+                        if (!is_esc) continue;
+                        const uint32_t hi = ln.byte();
+                        const uint32_t lo = ln.byte();
+                        const int32_t P = (int32_t)(int16_t)(uint16_t)((hi << 8) | lo);
+                        const int32_t mask = (i == 7) ? 3 : 1;
+                        if (((P - (int32_t)c) & mask) != 0) esc_bad = true;
+                        B[i] = P + 128;
+                    }
+                }
+                const int32_t px = B[0] ^ B[1] ^ B[2] ^ B[3] ^ B[4] ^ B[5] ^ B[6];
+                B[7] += px & 2;
+#pragma unroll
+                for (int i = 0; i < 8; i++) F[i] = kMagicF + (uint32_t)B[i];
+            } else {
+                const uint32_t px = e[0] ^ e[1] ^ e[2] ^ e[3] ^ e[4] ^ e[5] ^ e[6];
+                e[7] += px & 0x02000000u;
+#pragma unroll
+                for (int i = 0; i < 8; i++) F[i] = __byte_perm(e[i], kMagicF, 0x7653);
+            }
+            const float cst = -mult * kMagicQ;  // exact: mult has <= 7 significant bits
+            float y[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) y[i] = fmaf(__uint_as_float(F[i]), mult, cst);
+            if (active) {
+                if (KIND == K_BF16 || KIND == K_FP16) {
+                    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + eoff) =
+                        make_uint4(pack2(y[0], y[1], KIND), pack2(y[2], y[3], KIND), pack2(y[4], y[5], KIND),
+                                   pack2(y[6], y[7], KIND));
+                } else if (KIND == K_FP8) {
+                    *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(a.out) + eoff) =
+                        make_uint2(pack4_fp8(y[0], y[1], y[2], y[3]), pack4_fp8(y[4], y[5], y[6], y[7]));
+                } else {
+                    *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(a.out) + eoff) =
+                        make_uint2(pack4_i8(y[0], y[1], y[2], y[3]), pack4_i8(y[4], y[5], y[6], y[7]));
+                }
+                if (DUMP) {
+                    uint2 s;
+                    s.x = (e[0] >> 24) | ((e[1] >> 24) << 8) | ((e[2] >> 24) << 16) | (e[3] & 0xFF000000u);
+                    s.y = (e[4] >> 24) | ((e[5] >> 24) << 8) | ((e[6] >> 24) << 16) | (u7 << 24);
+                    *reinterpret_cast<uint2*>(a.sym_out + eoff) = s;
+                }
+            }
+        }
+        if (active && (ln.x != kRansL || ln.wp != ln.wend)) flag(status, EP_STATUS_LANE_END);
+        if (esc_bad) flag(status, EP_STATUS_ESCAPE);
+    }
+}
+
+__device__ __forceinline__ void copy_row_scales(const DecodeArgs& a, int64_t first, int64_t stride) {
+    if (a.scale_out)
+        for (int64_t r = first; r < a.rows; r += stride) a.scale_out[r] = a.t[r];
+}
+
+// ------------------------------------------------------------ single stream
+template <int KIND, bool DUMP>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a) {
+    extern __shared__ uint32_t smem[];
+    uint32_t* tab = smem;                    // n_ctx x 4096
+    uint32_t* fr = smem + a.n_ctx * kSlots;  // n_ctx x 256
+    uint32_t* cu = fr + a.n_ctx * 256;       // n_ctx x 256
+    build_tables(a, tab, fr, cu);
+    if (KIND == K_FP8 || KIND == K_INT8)
+        copy_row_scales(a, (int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
+    const int64_t n_groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
+    const int64_t warp_id = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+    const int64_t n_warps = (int64_t)gridDim.x * kWarpsPerCta;
+    for (int64_t grp = warp_id; grp < n_groups; grp += n_warps) decode_group<KIND, DUMP>(a, tab, grp, a.status);
+}
+
+// ----------------------------------------------------------------- batched
+// Many streams (e.g. every linear layer of a model) in one persistent launch.
+// Work unit = 16 tile groups (one per warp) of one stream; CTAs claim units in
+// stream order from a global counter, rebuild their tables when the stream
+// changes, and count finished units per stream.  With ring = R > 0, stream i
+// may share its output buffer with stream i - R ("decode back to back into
+// reused buffers"): a unit of stream i first waits (bounded) until every unit
+// of stream i - R is finished.  Claims are made only by running CTAs and in
+// stream order, so every awaited unit is held by a running CTA: no deadlock.
+struct BatchCounters {
+    unsigned long long claim;
+    uint32_t pad[2];
+    // followed by uint32_t done[n_items]
+};
+
+constexpr uint32_t kWaitSpins = 1u << 23;  // x ~256 ns sleep: about 2 s before giving up
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 2)
+    batch_kernel(const DecodeArgs* __restrict__ items, const int64_t* __restrict__ unit_start, int64_t n_items,
+                 int32_t ring, BatchCounters* ctr, uint32_t* status) {
+    extern __shared__ uint32_t smem[];
+    __shared__ int64_t s_unit, s_item;
+    __shared__ int s_skip;
+    uint32_t* done = reinterpret_cast<uint32_t*>(ctr + 1);
+    const int64_t total = unit_start[n_items];
+    int64_t cur = -1;
+    for (;;) {
+        if (threadIdx.x == 0) {
+            const int64_t u = (int64_t)atomicAdd(&ctr->claim, 1ull);
+            int64_t lo = 0, hi = n_items - 1;  // item with unit_start[item] <= u < unit_start[item + 1]
+            while (lo < hi) {
+                const int64_t mid = (lo + hi + 1) >> 1;
+                if (unit_start[mid] <= u) lo = mid; else hi = mid - 1;
+            }
+            s_unit = u;
+            s_item = lo;
+            s_skip = 0;
+            if (u < total && ring > 0 && lo >= ring) {
+                const int64_t prev = lo - ring;
+                const uint32_t need = (uint32_t)(unit_start[prev + 1] - unit_start[prev]);
+                uint32_t spins = 0;
+                while (*reinterpret_cast<volatile uint32_t*>(done + prev) < need && spins < kWaitSpins) {
+                    __nanosleep(256);
+                    spins++;
+                }
+                if (spins >= kWaitSpins) {
+                    atomicOr(status, EP_STATUS_WAIT_TIMEOUT);
+                    s_skip = 1;
+                }
+                __threadfence();
+            }
+        }
+        __syncthreads();
+        const int64_t unit = s_unit, item = s_item;
+        if (unit >= total) break;
+        const DecodeArgs& a = items[item];
+        uint32_t* tab = smem;
+        if (item != cur) {
+            build_tables(a, tab, smem + a.n_ctx * kSlots, smem + a.n_ctx * kSlots + a.n_ctx * 256);
+            cur = item;
+        }
+        const int64_t grp = (unit - unit_start[item]) * kWarpsPerCta + (threadIdx.x >> 5);
+        const int64_t n_groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
+        if (!s_skip && grp < n_groups) decode_group<KIND, false>(a, tab, grp, status);
+        if ((KIND == K_FP8 || KIND == K_INT8) && unit == unit_start[item])
+            copy_row_scales(a, threadIdx.x, blockDim.x);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atomicAdd(done + item, 1u);
+        }
+    }
+}
+
+// ------------------------------------------------------------ launching
+struct DeviceInfo {
+    int sms = 0;
+};
+
+DeviceInfo device_info() {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> g(mu);
+    if (dev < 0 || dev >= 64) return DeviceInfo{148};
+    if (!cache[dev].sms) cudaDeviceGetAttribute(&cache[dev].sms, cudaDevAttrMultiProcessorCount, dev);
+    return cache[dev];
+}
+
+template <int KIND, bool DUMP>
+ep_status launch(const DecodeArgs& a, size_t smem, cudaStream_t stream) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(decode_kernel<KIND, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)(ep::kLossyContexts * (kSlots + 512) * 4));
+    });
+    if (attr_err != cudaSuccess) return EP_ERR_CUDA;
+    const int64_t groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
+    const int64_t want = (groups + kWarpsPerCta - 1) / kWarpsPerCta;
+    const int64_t cap = 2ll * device_info().sms;
+    const int grid = (int)(want < cap ? want : cap);
+    decode_kernel<KIND, DUMP><<<grid, kThreads, smem, stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+size_t batch_layout(int64_t n, size_t* items_off, size_t* units_off, size_t* ctr_off) {
+    auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    *items_off = 0;
+    *units_off = up(sizeof(DecodeArgs) * (size_t)n);
+    *ctr_off = up(*units_off + sizeof(int64_t) * (size_t)(n + 1));
+    return up(*ctr_off + sizeof(BatchCounters) + sizeof(uint32_t) * (size_t)n);
+}
+
+ep_status fill_args(const uint8_t* h_blob, const void* d_blob, size_t bytes, void* d_out, float* d_scale,
+                    uint8_t* d_sym, uint32_t* d_status, Layout& L, DecodeArgs* a) {
+    if (!h_blob || !d_blob || !d_out) return EP_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(d_blob) | reinterpret_cast<uintptr_t>(d_out)) & 15u) return EP_ERR_INVALID_ARG;
+    if (d_sym && (reinterpret_cast<uintptr_t>(d_sym) & 7u)) return EP_ERR_INVALID_ARG;
+    ep_status st = parse_and_validate(h_blob, bytes, &L);
+    if (st != EP_OK) return st;
+    std::memset(a, 0, sizeof(*a));
+    const uint8_t* db = static_cast<const uint8_t*>(d_blob);
+    a->blob = db;
+    a->tile_off = reinterpret_cast<const uint64_t*>(db + L.offsets_off);
+    a->payload = db + L.payload_off;
+    a->payload_bytes = L.total - L.payload_off;
+    a->g = reinterpret_cast<const float*>(db + L.rowmeta_off);
+    a->m = a->g + L.rows;
+    a->t = a->g + 2 * L.rows;
+    for (int c = 0; c < L.n_ctx; c++) a->ctx_off[c] = (uint32_t)L.ctx_off[c];
+    a->n_ctx = L.n_ctx;
+    a->out = d_out;
+    a->scale_out = d_scale;
+    a->sym_out = d_sym;
+    a->status = d_status;
+    a->rows = L.rows;
+    a->cols = L.cols;
+    a->n_tiles = L.n_tiles;
+    a->tiles_per_row = L.cols / kTileCols;
+    return EP_OK;
+}
+
+int kind_of(const Layout& L) { return L.mode == EP_MODE_LOSSLESS_TILEANS ? K_LOSSLESS : L.container; }
+
+template <int KIND>
+ep_status launch_batch(const ep_batch_plan* p, uint32_t* d_status, cudaStream_t stream) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(batch_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)(ep::kLossyContexts * (kSlots + 512) * 4));
+    });
+    if (attr_err != cudaSuccess) return EP_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(p->d_workspace);
+    const size_t smem = (size_t)p->n_ctx * (kSlots + 512) * 4;
+    const int64_t cap = 2ll * device_info().sms;
+    const int grid = (int)(p->total_units < cap ? p->total_units : cap);
+    if (grid <= 0) return EP_OK;
+    batch_kernel<KIND><<<grid, kThreads, smem, stream>>>(
+        reinterpret_cast<const DecodeArgs*>(ws + p->items_off), reinterpret_cast<const int64_t*>(ws + p->units_off),
+        p->n_items, p->ring, reinterpret_cast<BatchCounters*>(ws + p->counters_off), d_status);
+    return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+ep_status decode_impl(const uint8_t* h_blob, const void* d_blob, size_t bytes, void* d_out, float* d_scale,
+                      uint8_t* d_sym, uint32_t* d_status, cudaStream_t stream) {
+    if (!d_status) return EP_ERR_INVALID_ARG;
+    thread_local Layout L;
+    DecodeArgs a;
+    ep_status st = fill_args(h_blob, d_blob, bytes, d_out, d_scale, d_sym, d_status, L, &a);
+    if (st != EP_OK) return st;
+    if (cudaMemsetAsync(d_status, 0, sizeof(uint32_t), stream) != cudaSuccess) return EP_ERR_CUDA;
+    const size_t smem = (size_t)L.n_ctx * (kSlots + 512) * 4;
+    const bool dump = d_sym != nullptr;
+    switch (kind_of(L)) {
+        case K_BF16: return dump ? launch<K_BF16, true>(a, smem, stream) : launch<K_BF16, false>(a, smem, stream);
+        case K_FP16: return dump ? launch<K_FP16, true>(a, smem, stream) : launch<K_FP16, false>(a, smem, stream);
+        case K_FP8: return dump ? launch<K_FP8, true>(a, smem, stream) : launch<K_FP8, false>(a, smem, stream);
+        case K_INT8: return dump ? launch<K_INT8, true>(a, smem, stream) : launch<K_INT8, false>(a, smem, stream);
+        default: return dump ? launch<K_LOSSLESS, true>(a, smem, stream) : launch<K_LOSSLESS, false>(a, smem, stream);
+    }
+}
+
+}  // namespace
+}  // namespace ep
+
+extern "C" {
+
+ep_status ep_decode(const uint8_t* h_blob, const void* d_blob, size_t bytes, void* d_out, float* d_row_scale_out,
+                    uint32_t* d_status, ep_stream_t stream) {
+    return ep::decode_impl(h_blob, d_blob, bytes, d_out, d_row_scale_out, nullptr, d_status,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+ep_status ep_decode_symbols(const uint8_t* h_blob, const void* d_blob, size_t bytes, void* d_out,
+                            float* d_row_scale_out, uint8_t* d_sym_out, uint32_t* d_status, ep_stream_t stream) {
+    if (!d_sym_out) return EP_ERR_INVALID_ARG;
+    return ep::decode_impl(h_blob, d_blob, bytes, d_out, d_row_scale_out, d_sym_out, d_status,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t ep_batch_workspace_bytes(int64_t n_items) {
+    if (n_items <= 0) return 0;
+    size_t a, b, c;
+    return ep::batch_layout(n_items, &a, &b, &c);
+}
+
+ep_status ep_batch_prepare(const ep_batch_item* items, int64_t n_items, int32_t ring, void* d_workspace,
+                           size_t workspace_bytes, ep_batch_plan* plan) {
+    using namespace ep;
+    if (!items || n_items <= 0 || !d_workspace || !plan || ring < 0) return EP_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(d_workspace) & 255u) return EP_ERR_INVALID_ARG;
+    size_t items_off, units_off, ctr_off;
+    const size_t need = batch_layout(n_items, &items_off, &units_off, &ctr_off);
+    if (workspace_bytes < need) return EP_ERR_INVALID_ARG;
+    std::vector<DecodeArgs> args((size_t)n_items);
+    std::vector<int64_t> units((size_t)n_items + 1, 0);
+    Layout* L = new (std::nothrow) Layout();
+    if (!L) return EP_ERR_NOMEM;
+    int kind = -1, n_ctx = 0;
+    ep_status st = EP_OK;
+    for (int64_t i = 0; i < n_items && st == EP_OK; i++) {
+        const ep_batch_item& it = items[i];
+        // the batch kernel reports through the status word given to ep_batch_decode
+        st = fill_args(it.h_blob, it.d_blob, it.bytes, it.d_out, it.d_row_scale_out, nullptr, nullptr, *L,
+                       &args[(size_t)i]);
+        if (st != EP_OK) break;
+        const int k = kind_of(*L);
+        if (kind >= 0 && k != kind) st = EP_ERR_INVALID_ARG;  // one container/mode per batch
+        kind = k;
+        n_ctx = std::max(n_ctx, L->n_ctx);
+        const int64_t groups = (L->n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
+        units[(size_t)i + 1] = units[(size_t)i] + (groups + kWarpsPerCta - 1) / kWarpsPerCta;
+    }
+    delete L;
+    if (st != EP_OK) return st;
+    uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+    if (cudaMemcpy(ws + items_off, args.data(), sizeof(DecodeArgs) * args.size(), cudaMemcpyHostToDevice) !=
+            cudaSuccess ||
+        cudaMemcpy(ws + units_off, units.data(), sizeof(int64_t) * units.size(), cudaMemcpyHostToDevice) !=
+            cudaSuccess)
+        return EP_ERR_CUDA;
+    std::memset(plan, 0, sizeof(*plan));
+    plan->n_items = n_items;
+    plan->total_units = units[(size_t)n_items];
+    plan->ring = ring;
+    plan->kind = kind;
+    plan->n_ctx = n_ctx;
+    plan->d_workspace = d_workspace;
+    plan->workspace_bytes = workspace_bytes;
+    plan->items_off = items_off;
+    plan->units_off = units_off;
+    plan->counters_off = ctr_off;
+    return EP_OK;
+}
+
+ep_status ep_batch_decode(const ep_batch_plan* plan, uint32_t* d_status, ep_stream_t stream) {
+    using namespace ep;
+    if (!plan || !plan->d_workspace || !d_status || plan->n_items <= 0) return EP_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(plan->d_workspace);
+    const size_t ctr_bytes = sizeof(BatchCounters) + sizeof(uint32_t) * (size_t)plan->n_items;
+    if (cudaMemsetAsync(ws + plan->counters_off, 0, ctr_bytes, s) != cudaSuccess) return EP_ERR_CUDA;
+    if (cudaMemsetAsync(d_status, 0, sizeof(uint32_t), s) != cudaSuccess) return EP_ERR_CUDA;
+    switch (plan->kind) {
+        case K_BF16: return launch_batch<K_BF16>(plan, d_status, s);
+        case K_FP16: return launch_batch<K_FP16>(plan, d_status, s);
+        case K_FP8: return launch_batch<K_FP8>(plan, d_status, s);
+        case K_INT8: return launch_batch<K_INT8>(plan, d_status, s);
+        case K_LOSSLESS: return launch_batch<K_LOSSLESS>(plan, d_status, s);
+    }
+    return EP_ERR_INVALID_ARG;
+}
+
+ep_status ep_sync_status(const uint32_t* d_status, ep_stream_t stream) {
+    if (!d_status) return EP_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t h = 0;
+    if (cudaMemcpyAsync(&h, d_status, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return EP_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return EP_ERR_CUDA;
+    return h ? EP_ERR_CORRUPT : EP_OK;
+}
+
+}  // extern "C"

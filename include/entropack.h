@@ -1,0 +1,186 @@
+/*
+ * entropack.h -- C ABI of libentropack.so, the B300 (sm_103a) implementation
+ * of EntroPack's inference hot path: on-GPU decoding of entropy-coded E8
+ * lattice weights into BF16 / FP16 / FP8 / INT8 containers, plus the host
+ * encoder that produces the stream.
+ *
+ * Method: "EntroPack: Fast and Accurate Entropy-Coded Weight Compression at
+ * Arbitrary Bitrates", Abstract -- row-normalised E8 lattice quantisation, a
+ * conditional probability model of lattice coordinates, sampled storage
+ * estimates to select the quantisation resolution, entropy coding in
+ * independently decodable tiles, fused symbol decoding and weight
+ * reconstruction on the GPU, containers BF16/FP16/FP8/INT8 with the storage
+ * bitrate independent of the container.
+ * API surface: "EntroPack PyTorch Guide: Lossless Weights, Bitrates and Memory
+ * Checks", sections "Choose a compression contract" (lossy target bitrate vs
+ * lossless tiled ANS; compress / decompress), "Start with a tensor round trip"
+ * (target_bpp vs actual_bpp, which includes metadata).
+ * The byte layout is fixed in FORMAT.md (version 1).
+ *
+ * Conventions
+ *  - Matrices are row-major; rows = out_features (M), cols = in_features (K).
+ *    Version 1 needs rows % 32 == 0 and cols % 128 == 0.
+ *  - Every pointer is owned by the caller, except the blob returned by
+ *    ep_encode (release it with ep_free).
+ *  - Device entry points are asynchronous on `stream`; they allocate nothing
+ *    and return EP_OK once the work is enqueued.  Corruption that only the
+ *    device can see (rANS end state, word counts, escape payloads, tile
+ *    bounds) is reported through the caller's status word; read it with
+ *    ep_sync_status.  Decoding never loops unboundedly: every loop is bounded
+ *    by the tile geometry.
+ *  - h_blob is a host copy of the stream (parsed and fully validated on the
+ *    host before any launch); d_blob must hold the same bytes on the device,
+ *    16-byte aligned.  The kernels re-check every tile's bounds, so a
+ *    mismatching device copy can only produce EP_ERR_CORRUPT, never an
+ *    out-of-bounds access.
+ */
+#ifndef ENTROPACK_H
+#define ENTROPACK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st *ep_stream_t;
+
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1, /* NULL pointer, misaligned pointer, bad enum, bad sizes */
+    EP_ERR_SHAPE = 2,       /* rows % 32 != 0 or cols % 128 != 0 or empty */
+    EP_ERR_NONFINITE = 3,   /* lossy input holds NaN or +-inf */
+    EP_ERR_CORRUPT = 4,     /* stream fails validation (host) or decoding (device status) */
+    EP_ERR_UNSUPPORTED = 5, /* value range outside format version 1 */
+    EP_ERR_NOMEM = 6,       /* host allocation failed (ep_encode only) */
+    EP_ERR_CUDA = 7         /* a CUDA runtime call failed */
+} ep_status;
+
+typedef enum { EP_C_BF16 = 0, EP_C_FP16 = 1, EP_C_FP8_E4M3 = 2, EP_C_INT8 = 3 } ep_container;
+typedef enum { EP_MODE_LOSSY_E8 = 0, EP_MODE_LOSSLESS_TILEANS = 1 } ep_mode;
+
+/* Device status-word bits (OR-ed by the kernels). */
+#define EP_STATUS_LANE_END 0x1u   /* a rANS lane did not end at L or did not consume exactly its words */
+#define EP_STATUS_TILE_BOUNDS 0x2u /* a tile offset or word count points outside the stream */
+#define EP_STATUS_ESCAPE 0x4u     /* an escape payload contradicts its coset */
+#define EP_STATUS_WAIT_TIMEOUT 0x8u /* ep_batch_decode: a ring wait gave up (about 2 s); that unit was skipped */
+
+typedef struct {
+    int32_t mode;      /* ep_mode */
+    float target_bpp;  /* lossy: target coded bits per parameter (> 0) */
+    int32_t container; /* ep_container of the decoded weights (lossless: EP_C_BF16) */
+    float sample_frac; /* fraction of rows sampled by the rate search; <= 0 selects 0.05 */
+    int32_t n_threads; /* host threads for ep_encode; <= 0 selects all hardware threads */
+} ep_params;
+
+typedef struct {
+    int64_t rows, cols, n_tiles;
+    int32_t mode, container;
+    float target_bpp;    /* as requested (lossy) */
+    int32_t j;           /* chosen resolution index: Delta = 2^(j/64) */
+    double delta;        /* Delta_j */
+    uint64_t total_bytes;
+    uint32_t n_sample_rows;
+    double actual_bpp;   /* 8 * total_bytes / (rows * cols): includes every byte of metadata */
+    size_t out_elem_bytes; /* bytes per decoded element (2 for BF16/FP16, 1 for FP8/INT8) */
+    int32_t has_row_scale; /* 1 when ep_decode also writes per-row output scales t_r */
+} ep_info;
+
+/* Library/format version (format 1). */
+int32_t ep_version(void);
+const char *ep_status_string(ep_status s);
+
+/*
+ * Host encoder.  w_bf16: rows x cols BF16 bit patterns (host memory).
+ * Lossy (p->mode == EP_MODE_LOSSY_E8): row-normalised E8 quantisation at the
+ * resolution whose sampled rate estimate is closest to p->target_bpp, then
+ * 12-bit rANS in 4-lane tiles of 32 x 128.  Lossless: exponent byte coded,
+ * sign+mantissa raw; decoding restores every bit.
+ * On success *blob points to *blob_bytes bytes allocated by the library
+ * (release with ep_free).  Errors: EP_ERR_INVALID_ARG, EP_ERR_SHAPE,
+ * EP_ERR_NONFINITE (lossy only), EP_ERR_UNSUPPORTED, EP_ERR_NOMEM.
+ */
+ep_status ep_encode(const uint16_t *w_bf16, int64_t rows, int64_t cols, const ep_params *p, uint8_t **blob,
+                    size_t *blob_bytes);
+void ep_free(void *p);
+
+/* 8 * bytes / (rows * cols) after validating the stream ("actual_bpp", metadata included). */
+ep_status ep_actual_bpp(const uint8_t *blob, size_t bytes, double *bpp);
+/* Parse and fully validate a host copy of a stream. */
+ep_status ep_query(const uint8_t *blob, size_t bytes, ep_info *out);
+
+/*
+ * Decode a stream on the GPU ("fused symbol decoding and numerical weight
+ * reconstruction on the GPU", Abstract).
+ *   d_out            rows x cols container elements, row-major, 16-byte aligned
+ *   d_row_scale_out  FP8/INT8 lossy streams: rows floats t_r such that
+ *                    weight[r, k] ~= t_r * d_out[r, k]; NULL allowed (and
+ *                    ignored) for BF16/FP16 and lossless streams
+ *   d_status         one u32, zeroed by this call (cudaMemsetAsync), then
+ *                    OR-ed with EP_STATUS_* bits by the kernel
+ * Returns EP_OK when the work is enqueued; host-side validation errors
+ * (EP_ERR_CORRUPT, EP_ERR_INVALID_ARG) return before any launch.
+ */
+ep_status ep_decode(const uint8_t *h_blob, const void *d_blob, size_t bytes, void *d_out, float *d_row_scale_out,
+                    uint32_t *d_status, ep_stream_t stream);
+
+/*
+ * Debug variant of ep_decode: also writes the coded symbol byte of every
+ * coordinate (rows x cols bytes, row-major) to d_sym_out; used to check the
+ * symbol stream against the CPU oracle bit for bit.
+ */
+ep_status ep_decode_symbols(const uint8_t *h_blob, const void *d_blob, size_t bytes, void *d_out,
+                            float *d_row_scale_out, uint8_t *d_sym_out, uint32_t *d_status, ep_stream_t stream);
+
+/*
+ * Batched decode: many streams (e.g. every linear layer of a model) in one
+ * persistent launch.  All items must share mode and container.  Work is cut
+ * into units of 128 tiles of one stream; CTAs claim units in item order.
+ *
+ *   ring == 0  every item writes its own d_out (outputs must not overlap);
+ *   ring == R  item i may reuse the output buffer of item i - R ("decode back
+ *              to back into reused buffers"): a unit of item i starts only
+ *              after every unit of item i - R has finished.  The wait is
+ *              bounded (about 2 s); on expiry the unit is skipped and
+ *              EP_STATUS_WAIT_TIMEOUT is set, so the call always returns.
+ *
+ * ep_batch_prepare validates every stream on the host and uploads the item
+ * descriptors into the caller's device workspace (d_workspace, 256-byte
+ * aligned, at least ep_batch_workspace_bytes(n_items) bytes) with a
+ * synchronous copy; the plan is a plain host struct.  ep_batch_decode then
+ * zeroes the workspace counters and *d_status on `stream` and launches one
+ * kernel; it may be called repeatedly (and captured in a CUDA graph) while
+ * the workspace, the streams and the outputs stay alive.  Calls that share a
+ * workspace must not overlap on the GPU.
+ */
+typedef struct {
+    const uint8_t *h_blob; /* host copy of the stream */
+    const void *d_blob;    /* device copy, 16-byte aligned */
+    size_t bytes;
+    void *d_out;            /* rows x cols container elements, 16-byte aligned */
+    float *d_row_scale_out; /* FP8/INT8: rows floats t_r (or NULL) */
+} ep_batch_item;
+
+typedef struct {
+    int64_t n_items, total_units;
+    int32_t ring, kind, n_ctx, reserved;
+    void *d_workspace;
+    size_t workspace_bytes;
+    uint64_t items_off, units_off, counters_off;
+} ep_batch_plan;
+
+size_t ep_batch_workspace_bytes(int64_t n_items);
+ep_status ep_batch_prepare(const ep_batch_item *items, int64_t n_items, int32_t ring, void *d_workspace,
+                           size_t workspace_bytes, ep_batch_plan *plan);
+ep_status ep_batch_decode(const ep_batch_plan *plan, uint32_t *d_status, ep_stream_t stream);
+
+/* Synchronise `stream` and map the status word: 0 -> EP_OK, any bit -> EP_ERR_CORRUPT. */
+ep_status ep_sync_status(const uint32_t *d_status, ep_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ENTROPACK_H */

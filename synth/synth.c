@@ -117,7 +117,9 @@ typedef struct { uint64_t kz, ku; double scale; uint16_t *out; } t5_ctx;
 static void t5_range(void *p, uint64_t lo, uint64_t hi) {
     t5_ctx *c = (t5_ctx *)p;
     for (uint64_t i = lo; i < hi; i++) {
-        double z = normal_at(c->kz, 2 * i), z2 = normal_at(c->kz, 2 * i + 1);
+        /* normals 2i and 2i+1 share one Box-Muller pair: compute it once */
+        double r = sqrt(-2.0 * log(u01(c->kz, 2 * i))), th = 6.283185307179586476925 * u01(c->kz, 2 * i + 1);
+        double z = r * cos(th), z2 = r * sin(th);
         double v = -2.0 * log(u01(c->ku, 2 * i) * u01(c->ku, 2 * i + 1)) + z2 * z2;
         c->out[i] = bf16_rne(c->scale * z / sqrt(v / 5.0));
     }

@@ -1,0 +1,147 @@
+"""Host-side checks of libentropack.so (no GPU needed).
+
+* the library loads and exports every function declared in include/entropack.h;
+* ep_encode (the library's own threaded C++ encoder) produces byte-identical
+  streams to the CPU oracle on the configured workloads (reduced sizes where
+  the oracle would take minutes);
+* ep_query / ep_actual_bpp / validation errors, and argument checks of the
+  device entry points that return before touching the GPU.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.conftest import ROOT
+
+
+def _ep():
+    import dit_weight_compression_02_b300 as ep
+    return ep
+
+
+def test_exports_every_declared_symbol():
+    from dit_weight_compression_02_b300 import _lib
+    hdr = open(os.path.join(ROOT, "include", "entropack.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    names = set(re.findall(r"\b(ep_[a-z_0-9]+)\s*\(", hdr))
+    assert len(names) >= 10, names
+    for n in sorted(names):
+        assert hasattr(_lib.lib, n), f"{n} declared in entropack.h but not exported"
+        assert n in _lib.SIGNATURES, f"{n} has no ctypes signature"
+    assert _lib.lib.ep_version() == 1
+
+
+CASES = [
+    ("c1_256x1024_n002_4bpp", lambda: synth.normal_bf16(1, 256, 1024), 4.0, "bf16"),
+    ("c2_1024x4096_rows_outliers_2p5", lambda: synth.rows_outliers_bf16(2, 1024, 4096), 2.5, "bf16"),
+    ("c2_1024x4096_rows_outliers_4p5", lambda: synth.rows_outliers_bf16(2, 1024, 4096), 4.5, "bf16"),
+    ("c3_q_3840x3840_t5_4bpp", lambda: synth.student_t5_bf16(3, 3840, 3840), 4.0, "bf16"),
+    ("c4_1024x2048_fp16_3bpp", lambda: synth.normal_bf16(4, 1024, 2048), 3.0, "fp16"),
+    ("c4_1024x2048_fp8_3bpp", lambda: synth.normal_bf16(4, 1024, 2048), 3.0, "fp8"),
+    ("c4_1024x2048_int8_3bpp", lambda: synth.normal_bf16(4, 1024, 2048), 3.0, "int8"),
+    ("escape_heavy_6bpp", lambda: synth.rows_outliers_bf16(9, 64, 512, frac=0.05, k_sigma=40.0), 6.0, "bf16"),
+    ("tiny_rows_and_zero_rows", lambda: _tiny_rows(), 3.5, "int8"),
+]
+
+
+def _tiny_rows():
+    w = synth.normal_bf16(10, 64, 256)
+    w[0] = 0
+    w[7] = synth.normal_bf16(11, 1, 256, std=1e-36)[0]
+    w[9] = 0x0001  # smallest subnormal everywhere
+    return w
+
+
+@pytest.mark.parametrize("name,gen,target,container", CASES, ids=[c[0] for c in CASES])
+def test_encoder_byte_identical_to_oracle(name, gen, target, container):
+    ep = _ep()
+    w = gen()
+    b_lib = ep.encode(w, target, container)
+    b_orc = oracle.encode(w, target, container)
+    assert len(b_lib) == len(b_orc)
+    assert b_lib == b_orc
+    q = ep.query(b_lib)
+    assert q["rows"] == w.shape[0] and q["cols"] == w.shape[1]
+    assert q["actual_bpp"] == pytest.approx(8 * len(b_lib) / w.size)
+    assert ep.actual_bpp(b_lib) == q["actual_bpp"]
+
+
+def test_encoder_thread_count_does_not_change_bytes():
+    ep = _ep()
+    w = synth.rows_outliers_bf16(12, 512, 1024)
+    ref = ep.encode(w, 3.5, n_threads=1)
+    for t in (2, 3, 7):
+        assert ep.encode(w, 3.5, n_threads=t) == ref
+
+
+def test_lossless_byte_identical_and_exhaustive():
+    ep = _ep()
+    w = synth.with_special_rows(synth.normal_bf16(4, 512, 1024), seed=4)
+    assert ep.encode(w, lossless=True) == oracle.encode_lossless(w)
+    every = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(512, 128)
+    assert ep.encode(every, lossless=True) == oracle.encode_lossless(every)
+
+
+def test_errors():
+    ep = _ep()
+    w = synth.normal_bf16(5, 64, 256)
+    bad = w.copy()
+    bad[3, 3] = 0x7F80
+    with pytest.raises(ep.EntroPackError) as e:
+        ep.encode(bad)
+    assert e.value.status == "EP_ERR_NONFINITE"
+    with pytest.raises(ep.EntroPackError) as e:
+        ep.encode(w[:, :200].copy())
+    assert e.value.status == "EP_ERR_SHAPE"
+    with pytest.raises(ep.EntroPackError) as e:
+        ep.encode(w, target_bpp=-1.0)
+    assert e.value.status == "EP_ERR_INVALID_ARG"
+    # lossless accepts non-finite values
+    assert oracle.decode(ep.encode(bad, lossless=True))[0][3, 3] == 0x7F80
+
+
+def _flip(blob, pos, mask=0x5A):
+    b = bytearray(blob)
+    b[pos] ^= mask
+    return bytes(b)
+
+
+def test_query_rejects_corrupt_headers_and_layouts():
+    ep = _ep()
+    blob = ep.encode(synth.normal_bf16(6, 64, 256), 4.0)
+    h = oracle.header(blob)
+    for pos in (0, 4, 6, 7, 8, 16, 24, 48, 52, 53, 56, 64, 72, 80, 88,  # header fields
+                h["tables_off"] + 2, h["offsets_off"] + 8, h["offsets_off"] + 8 * h["n_tiles"],
+                h["payload_off"] + 16):  # a lane word count
+        with pytest.raises(ep.EntroPackError) as e:
+            ep.query(_flip(blob, pos))
+        assert e.value.status == "EP_ERR_CORRUPT", pos
+    with pytest.raises(ep.EntroPackError):
+        ep.query(blob[:-16])
+    with pytest.raises(ep.EntroPackError):
+        ep.query(blob[:100])
+
+
+def test_device_entry_points_validate_before_launch():
+    """Errors found on the host return before any CUDA call (safe without a GPU)."""
+    ep = _ep()
+    from dit_weight_compression_02_b300._lib import lib
+    blob = ep.encode(synth.normal_bf16(7, 64, 256), 4.0)
+    host = np.frombuffer(blob, dtype=np.uint8)
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+    status = ctypes.c_void_p(1 << 21)
+    # misaligned device pointers
+    assert lib.ep_decode(host.ctypes.data, ctypes.c_void_p((1 << 20) + 8), len(blob), fake, None, status, None) == 1
+    # corrupt host copy
+    bad = np.frombuffer(_flip(blob, 0), dtype=np.uint8)
+    assert lib.ep_decode(bad.ctypes.data, fake, len(blob), fake, None, status, None) == 4
+    assert lib.ep_decode(host.ctypes.data, fake, len(blob) - 16, fake, None, status, None) == 4
+    assert lib.ep_decode(host.ctypes.data, fake, len(blob), fake, None, None, None) == 1
+    assert lib.ep_sync_status(None, None) == 1
+    assert lib.ep_batch_workspace_bytes(0) == 0
+    assert lib.ep_batch_workspace_bytes(5) > 0
