@@ -136,7 +136,11 @@ def run_ours(args, rank, world, device):
     import torch
 
     import synth
-    from dit_weight_compression_02_b300 import build as lib_build
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_entropack_build", os.path.join(ROOT, "dit_weight_compression_02_b300", "build.py"))
+    lib_build = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(lib_build)
     lib_build.build()
     import dit_weight_compression_02_b300 as ep
 
