@@ -5,19 +5,23 @@
 // reconstruction on the GPU"; containers BF16, FP16, FP8, INT8).
 //
 // Work decomposition.  A tile (32 x 128 weights) carries 4 independent rANS
-// lanes; one thread owns one lane, so one warp decodes 8 tiles.  Every CTA
-// first expands the stream's 12-bit frequency tables into 4096-entry slot
-// tables in shared memory (one u32 per slot: symbol byte | f | slot - cum),
-// then its warps walk tile groups.  A lane decodes its 128 blocks of 8
-// coordinates in the format's order; lanes 2h and 2h+1 of a tile write the two
-// halves of one 32-byte row segment, so each warp-wide 128-bit store covers
-// whole sectors.  Escapes (values beyond the direct byte range) are rare: the
-// fast path is branch-free and a warp-uniform test sends a block with any
-// escape through the slow path.
+// lanes; one thread owns one lane, so one warp decodes a group of 8 tiles.
+// A CTA is 1024 threads, one per SM: its 32 warps share one copy of the
+// stream's slot tables in shared memory (one u32 per 12-bit slot), which
+// leaves most of the SM's 256 KB L1 to cache the 1024 lane word streams
+// (each lane reads its 16-bit words in order, 16 words per 32-byte sector).
+// A lane decodes its 128 blocks of 8 coordinates in the format's order; lanes
+// 2h and 2h+1 of a tile write the two halves of one 32-byte row segment, so
+// every warp-wide 128-bit store covers whole sectors.  Escapes (values beyond
+// the direct byte range) are rare: the fast path is branch-free and a
+// warp-uniform test sends a block with any escape through the slow path.
 //
-// Reconstruction uses the format's 7-bit row steps: the symbol byte u = 2q+128
-// is spliced into the float 0x4AC00000 + u (= 6291520 + q) and one FMA with
-// c = -g * 6291520 (exact) yields fp32(g * q) with a single rounding.
+// Slot entry: f << 20 | u << 12 | (slot - cum_u), with f the 12-bit frequency
+// and u the symbol byte.  One LDS, one shift, one AND and one IMAD advance
+// the state.  Reconstruction: for a coordinate u = 2q + 128, the float with
+// bits (e & 0xFF000) | bits(1536.0f) has the value 1536 + u/2 = 1600 + q, so
+// fma(F, g, -1600 g) is fp32(g * q) rounded once (1600 g is exact because
+// the format's row steps and multipliers carry at most 7 significant bits).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -34,12 +38,14 @@
 namespace ep {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 1024;
 constexpr int kWarpsPerCta = kThreads / 32;
 constexpr int kTilesPerWarp = 8;
 constexpr int kSlots = 4096;
-constexpr uint32_t kMagicF = 0x4AC00000u;  // float 6291456 = 1.5 * 2^22 (spacing 0.5)
-constexpr float kMagicQ = 6291520.0f;       // 6291456 + 128 / 2
+constexpr uint32_t kMagicLo = 0x44C00000u;  // 1536.0f: bits 12..19 carry u, worth u/2
+constexpr float kMagicLoQ = 1600.0f;        // 1536 + 128/2
+constexpr uint32_t kMagicHi = 0x4AC00000u;  // 6291456.0f (spacing 0.5): escape path, any int16 payload
+constexpr float kMagicHiQ = 6291520.0f;     // 6291456 + 128/2
 
 enum Kind { K_BF16 = 0, K_FP16 = 1, K_FP8 = 2, K_INT8 = 3, K_LOSSLESS = 4 };
 
@@ -62,7 +68,12 @@ struct DecodeArgs {
 };
 
 // ---------------------------------------------------------------- tables
-// Expand (lo, n, f[n]) records into slot tables: entry = u << 24 | f << 12 | (slot - cum).
+// Expand the stream's (lo, n, f[n]) records into 4096-entry slot tables.
+// Scratch `fr` / `cu` (n_ctx x 256 u32 each) hold frequencies and cumulative
+// frequencies.  Every thread fills slots s = tid, tid + blockDim, ... of each
+// context by a binary search for the largest u with cum[u] <= s (that symbol
+// has f > 0 and covers s); neighbouring lanes take the same search path, so
+// the cum reads broadcast and the table stores are conflict-free.
 __device__ void build_tables(const DecodeArgs& a, uint32_t* tab, uint32_t* fr, uint32_t* cu) {
     const int n_ctx = a.n_ctx;
     for (int i = threadIdx.x; i < n_ctx * 256; i += blockDim.x) fr[i] = 0;
@@ -86,7 +97,7 @@ __device__ void build_tables(const DecodeArgs& a, uint32_t* tab, uint32_t* fr, u
         }
         uint32_t incl = s;
         for (int d = 1; d < 32; d <<= 1) {
-            uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+            const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
             if (lane >= d) incl += o;
         }
         uint32_t run = incl - s;
@@ -96,45 +107,42 @@ __device__ void build_tables(const DecodeArgs& a, uint32_t* tab, uint32_t* fr, u
         }
     }
     __syncthreads();
-    // chunks of 32 consecutive slots: binary search the first, then walk
-    for (int ch = threadIdx.x; ch < n_ctx * (kSlots / 32); ch += blockDim.x) {
-        const int c = ch / (kSlots / 32);
-        const uint32_t s0 = (uint32_t)(ch % (kSlots / 32)) * 32u;
+    for (int i = threadIdx.x; i < n_ctx * kSlots; i += blockDim.x) {
+        const int c = i / kSlots;
+        const uint32_t s = (uint32_t)(i % kSlots);
         const uint32_t* C = cu + c * 256;
-        const uint32_t* F = fr + c * 256;
-        int lo = 0, hi = 255;  // largest u with cum[u] <= s0
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (C[mid] <= s0) lo = mid; else hi = mid - 1;
-        }
-        int u = lo;
-        for (uint32_t s = s0; s < s0 + 32u; s++) {
-            while (u < 255 && s >= C[u] + F[u]) u++;
-            tab[c * kSlots + s] = ((uint32_t)u << 24) | (F[u] << 12) | ((s - C[u]) & 0xFFFu);
-        }
+        int u = 0;  // C[0] = 0 <= s; the steps sum to 255, so u + step never passes 255
+#pragma unroll
+        for (int step = 128; step >= 1; step >>= 1)
+            if (C[u + step] <= s) u += step;
+        tab[i] = (fr[c * 256 + u] << 20) | ((uint32_t)u << 12) | ((s - C[u]) & 0xFFFu);
     }
     __syncthreads();
 }
 
 // ---------------------------------------------------------------- rANS lane
+// State x in [2^16, 2^32) before every symbol; `next` is the word at index wi
+// of the lane's wn words (prefetched).  The refill is branch-free: the word
+// is spliced in with one byte permute and the prefetch of the following word
+// is predicated.  A corrupt lane never reads past its own words; it ends with
+// x != L or wi != wn and is reported.
 struct Lane {
-    uint32_t x;            // state
-    uint32_t next;         // next renormalisation word (prefetched)
-    const uint16_t* wp;    // position of `next` in the lane's words
-    const uint16_t* wend;  // one past the lane's last word
-    const uint16_t* safe;  // in-bounds address used once the lane is exhausted
+    uint32_t x;
+    uint32_t next;
+    uint32_t wi, wn;
+    const uint16_t* w;
 
     __device__ __forceinline__ void refill() {
-        if (x < kRansL) {
-            x = (x << 16) | next;
-            ++wp;
-            next = __ldg(wp < wend ? wp : safe);
-        }
+        const bool p = x < kRansL;
+        const uint32_t xr = __byte_perm(next, x, 0x5410);  // (x << 16) | next
+        x = p ? xr : x;
+        wi += p ? 1u : 0u;
+        if (p && wi < wn) next = __ldg(w + wi);
     }
     // one table symbol; returns the slot entry
     __device__ __forceinline__ uint32_t sym(const uint32_t* tab) {
         const uint32_t e = tab[x & (kProbScale - 1)];
-        x = ((e >> 12) & 0xFFFu) * (x >> kProbBits) + (e & 0xFFFu);
+        x = (e >> 20) * (x >> kProbBits) + (e & 0xFFFu);
         refill();
         return e;
     }
@@ -148,6 +156,8 @@ struct Lane {
 };
 
 __device__ __forceinline__ void flag(uint32_t* status, uint32_t bits) { atomicOr(status, bits); }
+
+__device__ __forceinline__ uint32_t sym_byte(uint32_t e) { return (e >> 12) & 0xFFu; }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, int kind) {
     if (kind == K_BF16) {
@@ -174,61 +184,85 @@ __device__ __forceinline__ uint32_t pack4_i8(float a, float b, float c, float d)
     return i8(a) | (i8(b) << 8) | (i8(c) << 16) | (i8(d) << 24);
 }
 
+template <int KIND>
+__device__ __forceinline__ void store_block(void* out, int64_t eoff, const float* y) {
+    if (KIND == K_BF16 || KIND == K_FP16) {
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + eoff) =
+            make_uint4(pack2(y[0], y[1], KIND), pack2(y[2], y[3], KIND), pack2(y[4], y[5], KIND),
+                       pack2(y[6], y[7], KIND));
+    } else if (KIND == K_FP8) {
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(out) + eoff) =
+            make_uint2(pack4_fp8(y[0], y[1], y[2], y[3]), pack4_fp8(y[4], y[5], y[6], y[7]));
+    } else {
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(out) + eoff) =
+            make_uint2(pack4_i8(y[0], y[1], y[2], y[3]), pack4_i8(y[4], y[5], y[6], y[7]));
+    }
+}
+
+__device__ __forceinline__ void dump_syms(uint8_t* sym_out, int64_t eoff, const uint32_t* u) {
+    uint2 s;
+    s.x = u[0] | (u[1] << 8) | (u[2] << 16) | (u[3] << 24);
+    s.y = u[4] | (u[5] << 8) | (u[6] << 16) | (u[7] << 24);
+    *reinterpret_cast<uint2*>(sym_out + eoff) = s;
+}
+
 // ------------------------------------------------------------- one group
 // One warp decodes tile group `grp` (8 tiles, one rANS lane per thread).
-// Returns without touching memory for tiles past the end.
+// Every lane runs the same number of steps (inactive lanes decode from a
+// dummy state and store nothing), so warp votes are always uniform.
 template <int KIND, bool DUMP>
 __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t* tab, int64_t grp,
                                              uint32_t* status) {
     const int lane = threadIdx.x & 31, l = lane & 3, tig = lane >> 2;
     const int64_t K = a.cols;
     constexpr uint32_t kHdr = (KIND == K_LOSSLESS ? kRawBytesPerTile : 0) + kTileHeaderBytes;
-    const uint16_t* safe = reinterpret_cast<const uint16_t*>(a.payload);
-    {
-        const int64_t tile = grp * kTilesPerWarp + tig;
-        bool active = tile < a.n_tiles;
-        uint64_t o0 = 0, o1 = 0;
-        if (active) {
-            o0 = a.tile_off[tile];
-            o1 = a.tile_off[tile + 1];
-            if (o0 > o1 || o1 > a.payload_bytes || (o0 & 15u) || o1 - o0 < kHdr) {
-                if (l == 0) flag(status, EP_STATUS_TILE_BOUNDS);
-                active = false;
-            }
+    const int64_t tile = grp * kTilesPerWarp + tig;
+    bool active = tile < a.n_tiles;
+    uint64_t o0 = 0, o1 = 0;
+    if (active) {
+        o0 = a.tile_off[tile];
+        o1 = a.tile_off[tile + 1];
+        if (o0 > o1 || o1 > a.payload_bytes || (o0 & 15u) || o1 - o0 < kHdr) {
+            if (l == 0) flag(status, EP_STATUS_TILE_BOUNDS);
+            active = false;
         }
-        const uint8_t* tb = a.payload + (active ? o0 : 0);
-        const uint8_t* th = tb + (KIND == K_LOSSLESS ? kRawBytesPerTile : 0);
-        Lane ln;
-        ln.x = kRansL;
-        ln.safe = safe;
-        ln.wp = ln.wend = safe;
-        if (active) {
-            const uint2 nwv = *reinterpret_cast<const uint2*>(th + 16);
-            const uint32_t nw[4] = {nwv.x & 0xFFFFu, nwv.x >> 16, nwv.y & 0xFFFFu, nwv.y >> 16};
-            const uint32_t total = nw[0] + nw[1] + nw[2] + nw[3];
-            uint32_t before = 0;
-            for (int i = 0; i < 4; i++) before += (i < l) ? nw[i] : 0u;
-            if (kHdr + 2ull * total > o1 - o0) {
-                if (l == 0) flag(status, EP_STATUS_TILE_BOUNDS);
-                active = false;
-            } else {
-                ln.x = reinterpret_cast<const uint32_t*>(th)[l];
-                ln.wp = reinterpret_cast<const uint16_t*>(th + kTileHeaderBytes) + before;
-                const uint32_t mine = l == 0 ? nw[0] : (l == 1 ? nw[1] : (l == 2 ? nw[2] : nw[3]));
-                ln.wend = ln.wp + mine;
-            }
+    }
+    const uint8_t* tb = a.payload + (active ? o0 : 0);
+    const uint8_t* th = tb + (KIND == K_LOSSLESS ? kRawBytesPerTile : 0);
+    Lane ln;
+    ln.x = kRansL;
+    ln.wi = 0;
+    ln.wn = 0;
+    ln.w = reinterpret_cast<const uint16_t*>(a.payload);
+    if (active) {
+        const uint2 nwv = *reinterpret_cast<const uint2*>(th + 16);
+        const uint32_t nw[4] = {nwv.x & 0xFFFFu, nwv.x >> 16, nwv.y & 0xFFFFu, nwv.y >> 16};
+        const uint32_t total = nw[0] + nw[1] + nw[2] + nw[3];
+        uint32_t before = 0;
+        for (int i = 0; i < 4; i++) before += (i < l) ? nw[i] : 0u;
+        if (kHdr + 2ull * total > o1 - o0) {
+            if (l == 0) flag(status, EP_STATUS_TILE_BOUNDS);
+            active = false;
+        } else {
+            ln.x = reinterpret_cast<const uint32_t*>(th)[l];
+            ln.w = reinterpret_cast<const uint16_t*>(th + kTileHeaderBytes) + before;
+            ln.wn = l == 0 ? nw[0] : (l == 1 ? nw[1] : (l == 2 ? nw[2] : nw[3]));
         }
-        ln.next = __ldg(ln.wp < ln.wend ? ln.wp : safe);
+    }
+    ln.next = ln.wn > 0 ? __ldg(ln.w) : 0u;
 
-        const int64_t tr0 = (tile / a.tiles_per_row) * kTileRows;
-        const int64_t tc0 = (tile % a.tiles_per_row) * kTileCols;
-        // element offset of this lane's first block (row 2*0 + l/2, column 8*(l&1))
-        const int64_t base = (tr0 + (l >> 1)) * K + tc0 + 8 * (l & 1);
-        bool esc_bad = false;
+    const int64_t tr0 = (tile / a.tiles_per_row) * kTileRows;
+    const int64_t tc0 = (tile % a.tiles_per_row) * kTileCols;
+    // this lane's block of step j sits at tile row 2 (j % 16) + l / 2 and
+    // tile column 16 (j / 16) + 8 (l % 2)
+    const int64_t row0 = tr0 + (l >> 1);
+    const int64_t base = row0 * K + tc0 + 8 * (l & 1);
+    bool esc_bad = false;
 
-        for (int j = 0; j < kBlocksPerLane; j++) {
-            const int m2 = j & 15, slab = j >> 4;
-            const int64_t row = tr0 + 2 * m2 + (l >> 1);
+    for (int slab = 0; slab < 8; slab++) {
+        for (int m2 = 0; m2 < 16; m2++) {
+            const int j = slab * 16 + m2;
+            const int64_t row = row0 + 2 * m2;
             const int64_t eoff = base + (int64_t)(2 * m2) * K + 16 * slab;
             if (KIND == K_LOSSLESS) {
                 uint2 raw = make_uint2(0, 0);
@@ -241,18 +275,18 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
                 for (int h = 0; h < 4; h++) {
                     const uint32_t rw = (h < 2 ? raw.x : raw.y) >> (16 * (h & 1));
                     const uint32_t r0 = rw & 0xFFu, r1 = (rw >> 8) & 0xFFu;
-                    const uint32_t v0 = ((r0 & 0x80u) << 8) | ((e[2 * h] >> 24) << 7) | (r0 & 0x7Fu);
-                    const uint32_t v1 = ((r1 & 0x80u) << 8) | ((e[2 * h + 1] >> 24) << 7) | (r1 & 0x7Fu);
+                    const uint32_t v0 = ((r0 & 0x80u) << 8) | ((e[2 * h] >> 5) & 0x7F80u) | (r0 & 0x7Fu);
+                    const uint32_t v1 = ((r1 & 0x80u) << 8) | ((e[2 * h + 1] >> 5) & 0x7F80u) | (r1 & 0x7Fu);
                     w[h] = v0 | (v1 << 16);
                 }
                 if (active) {
                     *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + eoff) =
                         make_uint4(w[0], w[1], w[2], w[3]);
                     if (DUMP) {
-                        uint2 s;
-                        s.x = (e[0] >> 24) | ((e[1] >> 24) << 8) | ((e[2] >> 24) << 16) | (e[3] & 0xFF000000u);
-                        s.y = (e[4] >> 24) | ((e[5] >> 24) << 8) | ((e[6] >> 24) << 16) | (e[7] & 0xFF000000u);
-                        *reinterpret_cast<uint2*>(a.sym_out + eoff) = s;
+                        uint32_t u[8];
+#pragma unroll
+                        for (int i = 0; i < 8; i++) u[i] = sym_byte(e[i]);
+                        dump_syms(a.sym_out, eoff, u);
                     }
                 }
                 continue;
@@ -262,21 +296,23 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
             if (KIND == K_FP8 || KIND == K_INT8) mult = active ? __ldg(a.m + row) : 0.f;
             uint32_t e[8];
             e[0] = ln.sym(tab);
-            const uint32_t c = (e[0] >> 24) & 1u;
-            const uint32_t* t1 = tab + (1u + c) * kSlots;
+            const uint32_t* t1 = tab + kSlots + ((e[0] >> 12) & 1u) * kSlots;  // context 1 + c
 #pragma unroll
             for (int i = 1; i < 7; i++) e[i] = ln.sym(t1);
-            e[7] = ln.sym(tab + (3u + c) * kSlots);
-            const uint32_t u7 = e[7] >> 24;  // coded byte, before the parity increment
-            bool esc = e[0] < (2u << 24);
-#pragma unroll
-            for (int i = 1; i < 8; i++) esc |= e[i] < (1u << 24);
-            esc = esc && active;
+            e[7] = ln.sym(t1 + 2 * kSlots);  // context 3 + c
             uint32_t F[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) F[i] = (e[i] & 0x000FF000u) | kMagicLo;
+            bool esc = F[0] <= kMagicLo + 0x1000u;  // s0 byte 0 or 1
+#pragma unroll
+            for (int i = 1; i < 8; i++) esc |= F[i] == kMagicLo;  // byte 0
+            esc = esc && active;
+            float y[8];
             if (__any_sync(0xffffffffu, esc)) {
+                const uint32_t c = (e[0] >> 12) & 1u;
                 int32_t B[8];
 #pragma unroll
-                for (int i = 0; i < 8; i++) B[i] = (int32_t)(e[i] >> 24);
+                for (int i = 0; i < 8; i++) B[i] = (int32_t)sym_byte(e[i]);
                 if (esc) {
 #pragma unroll
                     for (int i = 0; i < 8; i++) {
@@ -292,41 +328,30 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
                 }
                 const int32_t px = B[0] ^ B[1] ^ B[2] ^ B[3] ^ B[4] ^ B[5] ^ B[6];
                 B[7] += px & 2;
+                const float cst = -mult * kMagicHiQ;  // exact: mult has <= 7 significant bits
 #pragma unroll
-                for (int i = 0; i < 8; i++) F[i] = kMagicF + (uint32_t)B[i];
+                for (int i = 0; i < 8; i++) y[i] = fmaf(__uint_as_float(kMagicHi + (uint32_t)B[i]), mult, cst);
             } else {
+                // parity of a_0..a_6 is bit 1 of the XOR of the symbol bytes (bit 13 of the entries)
                 const uint32_t px = e[0] ^ e[1] ^ e[2] ^ e[3] ^ e[4] ^ e[5] ^ e[6];
-                e[7] += px & 0x02000000u;
+                F[7] += px & 0x2000u;
+                const float cst = -mult * kMagicLoQ;  // exact: mult has <= 7 significant bits
 #pragma unroll
-                for (int i = 0; i < 8; i++) F[i] = __byte_perm(e[i], kMagicF, 0x7653);
+                for (int i = 0; i < 8; i++) y[i] = fmaf(__uint_as_float(F[i]), mult, cst);
             }
-            const float cst = -mult * kMagicQ;  // exact: mult has <= 7 significant bits
-            float y[8];
-#pragma unroll
-            for (int i = 0; i < 8; i++) y[i] = fmaf(__uint_as_float(F[i]), mult, cst);
             if (active) {
-                if (KIND == K_BF16 || KIND == K_FP16) {
-                    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + eoff) =
-                        make_uint4(pack2(y[0], y[1], KIND), pack2(y[2], y[3], KIND), pack2(y[4], y[5], KIND),
-                                   pack2(y[6], y[7], KIND));
-                } else if (KIND == K_FP8) {
-                    *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(a.out) + eoff) =
-                        make_uint2(pack4_fp8(y[0], y[1], y[2], y[3]), pack4_fp8(y[4], y[5], y[6], y[7]));
-                } else {
-                    *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(a.out) + eoff) =
-                        make_uint2(pack4_i8(y[0], y[1], y[2], y[3]), pack4_i8(y[4], y[5], y[6], y[7]));
-                }
+                store_block<KIND>(a.out, eoff, y);
                 if (DUMP) {
-                    uint2 s;
-                    s.x = (e[0] >> 24) | ((e[1] >> 24) << 8) | ((e[2] >> 24) << 16) | (e[3] & 0xFF000000u);
-                    s.y = (e[4] >> 24) | ((e[5] >> 24) << 8) | ((e[6] >> 24) << 16) | (u7 << 24);
-                    *reinterpret_cast<uint2*>(a.sym_out + eoff) = s;
+                    uint32_t u[8];
+#pragma unroll
+                    for (int i = 0; i < 8; i++) u[i] = sym_byte(e[i]);
+                    dump_syms(a.sym_out, eoff, u);
                 }
             }
         }
-        if (active && (ln.x != kRansL || ln.wp != ln.wend)) flag(status, EP_STATUS_LANE_END);
-        if (esc_bad) flag(status, EP_STATUS_ESCAPE);
     }
+    if (active && (ln.x != kRansL || ln.wi != ln.wn)) flag(status, EP_STATUS_LANE_END);
+    if (esc_bad) flag(status, EP_STATUS_ESCAPE);
 }
 
 __device__ __forceinline__ void copy_row_scales(const DecodeArgs& a, int64_t first, int64_t stride) {
@@ -335,8 +360,10 @@ __device__ __forceinline__ void copy_row_scales(const DecodeArgs& a, int64_t fir
 }
 
 // ------------------------------------------------------------ single stream
+// Tile groups are dealt round-robin over the CTAs first (group g goes to CTA
+// g % gridDim.x), so a small matrix still spreads over every SM.
 template <int KIND, bool DUMP>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a) {
     extern __shared__ uint32_t smem[];
     uint32_t* tab = smem;                    // n_ctx x 4096
     uint32_t* fr = smem + a.n_ctx * kSlots;  // n_ctx x 256
@@ -345,14 +372,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
     if (KIND == K_FP8 || KIND == K_INT8)
         copy_row_scales(a, (int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
     const int64_t n_groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
-    const int64_t warp_id = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-    const int64_t n_warps = (int64_t)gridDim.x * kWarpsPerCta;
-    for (int64_t grp = warp_id; grp < n_groups; grp += n_warps) decode_group<KIND, DUMP>(a, tab, grp, a.status);
+    const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta;
+    for (int64_t grp = (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x; grp < n_groups; grp += stride)
+        decode_group<KIND, DUMP>(a, tab, grp, a.status);
 }
 
 // ----------------------------------------------------------------- batched
 // Many streams (e.g. every linear layer of a model) in one persistent launch.
-// Work unit = 16 tile groups (one per warp) of one stream; CTAs claim units in
+// Work unit = 32 tile groups (one per warp) of one stream; CTAs claim units in
 // stream order from a global counter, rebuild their tables when the stream
 // changes, and count finished units per stream.  With ring = R > 0, stream i
 // may share its output buffer with stream i - R ("decode back to back into
@@ -368,7 +395,7 @@ struct BatchCounters {
 constexpr uint32_t kWaitSpins = 1u << 23;  // x ~256 ns sleep: about 2 s before giving up
 
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     batch_kernel(const DecodeArgs* __restrict__ items, const int64_t* __restrict__ unit_start, int64_t n_items,
                  int32_t ring, BatchCounters* ctr, uint32_t* status) {
     extern __shared__ uint32_t smem[];
@@ -426,6 +453,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // ------------------------------------------------------------ launching
+constexpr size_t kMaxSmem = (size_t)ep::kLossyContexts * (kSlots + 512) * 4;
+
 struct DeviceInfo {
     int sms = 0;
 };
@@ -447,13 +476,12 @@ ep_status launch(const DecodeArgs& a, size_t smem, cudaStream_t stream) {
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(decode_kernel<KIND, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)(ep::kLossyContexts * (kSlots + 512) * 4));
+                                        (int)kMaxSmem);
     });
     if (attr_err != cudaSuccess) return EP_ERR_CUDA;
     const int64_t groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
-    const int64_t want = (groups + kWarpsPerCta - 1) / kWarpsPerCta;
-    const int64_t cap = 2ll * device_info().sms;
-    const int grid = (int)(want < cap ? want : cap);
+    const int64_t cap = device_info().sms;
+    const int grid = (int)(groups < cap ? groups : cap);
     decode_kernel<KIND, DUMP><<<grid, kThreads, smem, stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
@@ -503,12 +531,12 @@ ep_status launch_batch(const ep_batch_plan* p, uint32_t* d_status, cudaStream_t 
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(batch_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)(ep::kLossyContexts * (kSlots + 512) * 4));
+                                        (int)kMaxSmem);
     });
     if (attr_err != cudaSuccess) return EP_ERR_CUDA;
     uint8_t* ws = static_cast<uint8_t*>(p->d_workspace);
     const size_t smem = (size_t)p->n_ctx * (kSlots + 512) * 4;
-    const int64_t cap = 2ll * device_info().sms;
+    const int64_t cap = device_info().sms;
     const int grid = (int)(p->total_units < cap ? p->total_units : cap);
     if (grid <= 0) return EP_OK;
     batch_kernel<KIND><<<grid, kThreads, smem, stream>>>(
@@ -538,7 +566,6 @@ ep_status decode_impl(const uint8_t* h_blob, const void* d_blob, size_t bytes, v
 
 }  // namespace
 }  // namespace ep
-
 extern "C" {
 
 ep_status ep_decode(const uint8_t* h_blob, const void* d_blob, size_t bytes, void* d_out, float* d_row_scale_out,
