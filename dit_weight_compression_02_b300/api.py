@@ -172,6 +172,51 @@ class BatchDecoder:
         sync_status(self.status, stream)
 
 
+# ------------------------------------------------------------------ linear
+LINEAR_DECODE_THEN_GEMM, LINEAR_FUSED = 0, 1
+
+
+def _check_bf16_2d(t: torch.Tensor, name: str) -> None:
+    if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D BF16 CUDA tensor")
+
+
+def linear_bf16(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None, status=None, stream=None):
+    """ep_linear_bf16: Y = X W^T on the tcgen05 GEMM (dense BF16 W)."""
+    _check_bf16_2d(x, "x")
+    _check_bf16_2d(w, "w")
+    if x.shape[1] != w.shape[1]:
+        raise ValueError("x and w disagree on in_features")
+    y = torch.empty((x.shape[0], w.shape[0]), dtype=torch.bfloat16, device=x.device) if out is None else out
+    st = torch.zeros(1, dtype=torch.int32, device=x.device) if status is None else status
+    check(lib.ep_linear_bf16(_ptr(x), _ptr(w), _ptr(y), x.shape[0], w.shape[0], w.shape[1], _ptr(st),
+                             _stream_handle(stream)), "ep_linear_bf16")
+    if status is None:
+        sync_status(st, stream)
+    return y
+
+
+def compressed_linear(db: DeviceBlob, x: torch.Tensor, mode: int = LINEAR_DECODE_THEN_GEMM,
+                      out: torch.Tensor | None = None, workspace: torch.Tensor | None = None, status=None,
+                      stream=None):
+    """ep_compressed_linear: Y = X W^T with W decoded from `db` by the library's kernels."""
+    _check_bf16_2d(x, "x")
+    rows, cols = db.shape
+    if x.shape[1] != cols:
+        raise ValueError("x does not match the stream's in_features")
+    y = torch.empty((x.shape[0], rows), dtype=torch.bfloat16, device=x.device) if out is None else out
+    if mode == LINEAR_DECODE_THEN_GEMM and workspace is None:
+        workspace = torch.empty(rows * cols, dtype=torch.bfloat16, device=x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = torch.zeros(1, dtype=torch.int32, device=x.device) if status is None else status
+    check(lib.ep_compressed_linear(_ptr(db.host), _ptr(db.device), db.nbytes, _ptr(x), x.shape[0], _ptr(y),
+                                   int(mode), _ptr(workspace), ws_bytes, _ptr(st), _stream_handle(stream)),
+          "ep_compressed_linear")
+    if status is None:
+        sync_status(st, stream)
+    return y
+
+
 # ------------------------------------------------------------ tensor-level API
 @dataclass
 class EntroPackLossyConfig:
@@ -223,8 +268,9 @@ def decompress(ct: CompressedTensor, stream=None):
 class CompressedLinear(torch.nn.Module):
     """Linear layer whose weight stays entropy-coded in HBM and is decoded on each call.
 
-    forward(x) = x @ W^T (+ bias) with W decoded into a BF16 workspace by the
-    library's kernel, then a BF16 GEMM.
+    forward(x) = x @ W^T (+ bias): ep_compressed_linear decodes W with the
+    library's decode kernel into a BF16 workspace and multiplies on the
+    tcgen05 GEMM kernel; any leading batch dimensions of x are flattened.
     """
 
     def __init__(self, ct: CompressedTensor, bias: torch.Tensor | None = None):
@@ -253,11 +299,16 @@ class CompressedLinear(torch.nn.Module):
         return self._ws
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:
-        w = self.decoded_weight()
-        y = torch.nn.functional.linear(x.to(torch.bfloat16), w)
+        dev = self.ct.blob.device.device
+        if self._ws is None:
+            self._ws = torch.empty(self.ct.shape, dtype=torch.bfloat16, device=dev)
+            self._status = torch.zeros(1, dtype=torch.int32, device=dev)
+        lead = x.shape[:-1]
+        x2 = x.reshape(-1, x.shape[-1]).to(torch.bfloat16).contiguous()
+        y = compressed_linear(self.ct.blob, x2, LINEAR_DECODE_THEN_GEMM, workspace=self._ws, status=self._status)
         if self.bias is not None:
             y = y + self.bias
-        return y
+        return y.reshape(*lead, self.out_features)
 
     def check_status(self):
         if self._status is not None:
@@ -265,5 +316,6 @@ class CompressedLinear(torch.nn.Module):
 
 
 __all__ = ["encode", "query", "actual_bpp", "DeviceBlob", "decode", "decode_into", "sync_status", "BatchDecoder",
+           "linear_bf16", "compressed_linear", "LINEAR_DECODE_THEN_GEMM", "LINEAR_FUSED",
            "EntroPackLossyConfig", "TileANSConfig", "CompressedTensor", "compress", "decompress",
            "CompressedLinear", "EntroPackError", "CONTAINERS", "CONTAINER_DTYPES"]

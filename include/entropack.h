@@ -176,6 +176,39 @@ ep_status ep_batch_prepare(const ep_batch_item *items, int64_t n_items, int32_t 
                            size_t workspace_bytes, ep_batch_plan *plan);
 ep_status ep_batch_decode(const ep_batch_plan *plan, uint32_t *d_status, ep_stream_t stream);
 
+/*
+ * Linear layers ("EntroPack PyTorch Guide", "Replace one linear layer before
+ * a whole model": CompressedLinear.from_linear).  Y = X * W^T with row-major
+ * BF16 X [tokens x cols], W [rows x cols] and Y [tokens x rows]; the product
+ * is accumulated in fp32 by tcgen05 tensor-core instructions and rounded to
+ * BF16 once.  Device pointers are caller-owned and 16-byte aligned; tokens
+ * may be any positive count, rows must be a multiple of 32 and cols of 8.
+ * d_status (one u32) is zeroed by the call; the kernel sets
+ * EP_STATUS_WAIT_TIMEOUT if an internal pipeline wait gives up (about 2 s),
+ * which never happens in a correct run.  Returns EP_OK once enqueued.
+ */
+typedef enum {
+    EP_LINEAR_DECODE_THEN_GEMM = 0, /* decode W into d_ws (rows x cols BF16), then the GEMM */
+    EP_LINEAR_FUSED = 1             /* decode W tiles straight into shared memory (no workspace) */
+} ep_linear_mode;
+
+/* Dense BF16 GEMM (uncompressed W): the tensor-core kernel used by ep_compressed_linear. */
+ep_status ep_linear_bf16(const uint16_t *d_x, const uint16_t *d_w, uint16_t *d_y, int64_t tokens, int64_t rows,
+                         int64_t cols, uint32_t *d_status, ep_stream_t stream);
+
+/*
+ * CompressedLinear forward on a lossy BF16 stream (h_blob / d_blob as for
+ * ep_decode; rows = out_features, cols = in_features).  mode
+ * EP_LINEAR_DECODE_THEN_GEMM needs d_ws of at least rows * cols * 2 bytes.
+ * Stream corruption found by the decoder shows up in d_status like
+ * ep_decode's.  Errors before launch: EP_ERR_INVALID_ARG, EP_ERR_SHAPE,
+ * EP_ERR_CORRUPT (host validation), EP_ERR_UNSUPPORTED (lossless or non-BF16
+ * stream, or a mode this build does not provide).
+ */
+ep_status ep_compressed_linear(const uint8_t *h_blob, const void *d_blob, size_t bytes, const uint16_t *d_x,
+                               int64_t tokens, uint16_t *d_y, int32_t mode, void *d_ws, size_t ws_bytes,
+                               uint32_t *d_status, ep_stream_t stream);
+
 /* Synchronise `stream` and map the status word: 0 -> EP_OK, any bit -> EP_ERR_CORRUPT. */
 ep_status ep_sync_status(const uint32_t *d_status, ep_stream_t stream);
 

@@ -1,0 +1,118 @@
+"""GPU checks of the tcgen05 linear kernels against the fp64 oracle GEMM.
+
+ep_linear_bf16 (dense BF16 W) and ep_compressed_linear (W decoded from a
+stream) compute Y = X W^T in fp32 and round Y to BF16 once.  The reference
+is the oracle's plain fp64 triple loop over the same BF16 X and the oracle's
+decode of W.  Bars:
+  * the CompressedLinear bar of max |Y - Y_ref| / max |Y_ref| <= 2e-2;
+  * elementwise |Y - Y_ref| <= 2^-8 |Y_ref| + 1e-6 * sum_k |x_k w_k|: one
+    BF16 rounding (2^-9 relative) plus fp32 accumulation over K terms;
+which a transposed operand, a wrong swizzle or a dropped K block all fail.
+Shapes span several tiles with ragged tails in every dimension; the full
+CompressedLinear size (8192 x 3840 by 10240 x 3840) is checked on sampled
+token rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ep():
+    import dit_weight_compression_02_b300 as m
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    return m
+
+
+def _bf16_dev(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).cuda()
+
+
+def _check(y: torch.Tensor, x_bits: np.ndarray, w64: np.ndarray, rows=None):
+    x64 = synth.bf16_to_f32(x_bits).astype(np.float64)
+    if rows is not None:
+        x64 = x64[rows]
+    y_ref = oracle.gemm_f64(x64, w64)
+    mag = oracle.gemm_f64(np.abs(x64), np.abs(w64))
+    yg = y.float().cpu().numpy().astype(np.float64)
+    if rows is not None:
+        yg = yg[rows]
+    err = np.abs(yg - y_ref)
+    assert err.max() / np.abs(y_ref).max() <= 2e-2
+    bound = 2.0 ** -8 * np.abs(y_ref) + 1e-6 * mag + 1e-30
+    bad = np.argwhere(err > bound)
+    assert bad.size == 0, f"{len(bad)} elements out of bound, first {bad[:5]} err {err[tuple(bad[0])]}"
+
+
+@pytest.mark.parametrize("T,N,K", [(128, 256, 64), (300, 544, 200), (257, 3840, 384), (1000, 512, 1024)])
+def test_dense_gemm_ragged(ep, T, N, K):
+    x = synth.normal_bf16(100 + T, T, K, std=1.0)
+    w = synth.student_t5_bf16(200 + N, N, K)
+    y = ep.linear_bf16(_bf16_dev(x), _bf16_dev(w))
+    _check(y, x, synth.bf16_to_f32(w).astype(np.float64))
+
+
+def test_dense_gemm_matches_torch_closely(ep):
+    x = synth.normal_bf16(7, 512, 1024, std=1.0)
+    w = synth.normal_bf16(8, 768, 1024)
+    xd, wd = _bf16_dev(x), _bf16_dev(w)
+    y = ep.linear_bf16(xd, wd).float()
+    ref = (xd.float() @ wd.float().t())
+    rel = ((y - ref).abs().max() / ref.abs().max()).item()
+    assert rel < 4e-3
+
+
+def test_compressed_linear_small(ep):
+    w = synth.student_t5_bf16(61, 1024, 3840)
+    x = synth.normal_bf16(62, 333, 3840, std=1.0)
+    blob = oracle.encode(w, 4.0)
+    db = ep.DeviceBlob(blob)
+    y = ep.compressed_linear(db, _bf16_dev(x))
+    w_hat = oracle.container_to_f64(oracle.decode(blob)[0], "bf16")
+    _check(y, x, w_hat)
+
+
+def test_compressed_linear_full_size_sampled(ep):
+    # X 8192 x 3840 N(0,1), W 10240 x 3840 Student-t at 4 bpp
+    w = synth.student_t5_bf16(5, 10240, 3840)
+    x = synth.normal_bf16(5, 8192, 3840, std=1.0)
+    blob = ep.encode(w, 4.0)
+    assert blob == oracle.encode(w, 4.0)
+    db = ep.DeviceBlob(blob)
+    y = ep.compressed_linear(db, _bf16_dev(x))
+    w_hat = oracle.container_to_f64(oracle.decode_threaded(blob)[0], "bf16")
+    rows = np.r_[0:16, 4090:4106, 8176:8192]
+    _check(y, x, w_hat, rows=rows)
+
+
+def test_compressed_linear_rejects_bad_args(ep):
+    w = synth.normal_bf16(63, 64, 256)
+    db = ep.DeviceBlob(oracle.encode(w, 4.0))
+    x = _bf16_dev(synth.normal_bf16(64, 16, 256))
+    with pytest.raises(ep.EntroPackError) as e:
+        ep.compressed_linear(db, x, workspace=torch.empty(10, dtype=torch.bfloat16, device="cuda"))
+    assert e.value.status == "EP_ERR_INVALID_ARG"
+    db8 = ep.DeviceBlob(oracle.encode(w, 3.0, "fp8"))
+    with pytest.raises(ep.EntroPackError) as e:
+        ep.compressed_linear(db8, x)
+    assert e.value.status == "EP_ERR_UNSUPPORTED"
+
+
+def test_compressed_linear_module(ep):
+    torch.manual_seed(0)
+    w = synth.student_t5_bf16(65, 512, 1024)
+    lin = torch.nn.Linear(1024, 512, bias=True)
+    with torch.no_grad():
+        lin.weight.copy_(torch.from_numpy(synth.bf16_to_f32(w)))
+    cl = ep.CompressedLinear.from_linear(lin, ep.EntroPackLossyConfig(4.0))
+    x = torch.randn(2, 50, 1024).to(torch.bfloat16).cuda()
+    y = cl(x)
+    assert y.shape == (2, 50, 512)
+    w_hat = torch.from_numpy(oracle.container_to_f64(oracle.decode(oracle.encode(w, 4.0))[0], "bf16")).cuda()
+    ref = x.double() @ w_hat.t() + lin.bias.detach().double().cuda()
+    assert ((y.double() - ref).abs().max() / ref.abs().max()).item() < 2e-2
