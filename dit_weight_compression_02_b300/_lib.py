@@ -57,6 +57,7 @@ SIGNATURES = {
     "ep_batch_prepare": (i32, [ctypes.POINTER(EpBatchItem), i64, i32, P, sz, ctypes.POINTER(EpBatchPlan)]),
     "ep_batch_decode": (i32, [ctypes.POINTER(EpBatchPlan), P, P]),
     "ep_sync_status": (i32, [P, P]),
+    "ep_batch_decode_static": (i32, [ctypes.POINTER(EpBatchItem), i64, i32, P, P]),
     "ep_linear_bf16": (i32, [P, P, P, i64, i64, i64, P, P]),
     "ep_compressed_linear": (i32, [P, P, sz, P, i64, P, i32, P, sz, P, P]),
 }

@@ -486,12 +486,18 @@ ep_status launch(const DecodeArgs& a, size_t smem, cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 
+constexpr size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
+constexpr size_t batch_units_off(int64_t n) { return up256(sizeof(DecodeArgs) * (size_t)n); }
+constexpr size_t batch_ctr_off(int64_t n) { return up256(batch_units_off(n) + sizeof(int64_t) * (size_t)(n + 1)); }
+constexpr size_t batch_bytes(int64_t n) {
+    return up256(batch_ctr_off(n) + sizeof(BatchCounters) + sizeof(uint32_t) * (size_t)n);
+}
+
 size_t batch_layout(int64_t n, size_t* items_off, size_t* units_off, size_t* ctr_off) {
-    auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
     *items_off = 0;
-    *units_off = up(sizeof(DecodeArgs) * (size_t)n);
-    *ctr_off = up(*units_off + sizeof(int64_t) * (size_t)(n + 1));
-    return up(*ctr_off + sizeof(BatchCounters) + sizeof(uint32_t) * (size_t)n);
+    *units_off = batch_units_off(n);
+    *ctr_off = batch_ctr_off(n);
+    return batch_bytes(n);
 }
 
 ep_status fill_args(const uint8_t* h_blob, const void* d_blob, size_t bytes, void* d_out, float* d_scale,
@@ -664,3 +670,118 @@ ep_status ep_sync_status(const uint32_t* d_status, ep_stream_t stream) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------ allocation-free batched decode
+// Some callers cannot allocate device memory at all: code that runs inside
+// another framework's memory pool or allocator lock, plug-ins loaded into a
+// host process that owns every allocation, or real-time paths where a
+// cudaMalloc would synchronise the device.  ep_batch_decode_static serves
+// them: the batch kernel's scratch (item descriptors, unit table, claim and
+// completion counters) lives in the file-scope device array below instead of
+// a caller workspace.  Every GPU that loads the library holds these bytes
+// until the process exits.
+namespace ep {
+namespace {
+constexpr int64_t kStaticMaxItems = EP_BATCH_STATIC_MAX_ITEMS;
+constexpr size_t kStaticScratchBytes = batch_bytes(kStaticMaxItems);
+}  // namespace
+}  // namespace ep
+
+static __device__ __align__(256) uint8_t g_ep_batch_scratch[ep::kStaticScratchBytes];
+
+namespace ep {
+namespace {
+
+// Device address of g_ep_batch_scratch on the current device.  In host code
+// the array's name only stands in for the symbol, so the address is looked up
+// once per device (with that device current) and cached.
+ep_status static_scratch_address(uint8_t** out) {
+    static std::mutex mu;
+    static uint8_t* cache[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return EP_ERR_CUDA;
+    std::lock_guard<std::mutex> g(mu);
+    if (!cache[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ep_batch_scratch) != cudaSuccess || !p) return EP_ERR_CUDA;
+        cache[dev] = static_cast<uint8_t*>(p);
+    }
+    *out = cache[dev];
+    return EP_OK;
+}
+
+}  // namespace
+}  // namespace ep
+
+extern "C" ep_status ep_batch_decode_static(const ep_batch_item* items, int64_t n_items, int32_t ring,
+                                            uint32_t* d_status, ep_stream_t stream) {
+    using namespace ep;
+    if (!items || n_items <= 0 || ring < 0 || !d_status) return EP_ERR_INVALID_ARG;
+    if (n_items > kStaticMaxItems) return EP_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = nullptr;
+    ep_status st = static_scratch_address(&ws);
+    if (st != EP_OK) return st;
+    const size_t units_off = batch_units_off(n_items), ctr_off = batch_ctr_off(n_items);
+
+    // Validate every stream and stage the descriptors in fixed-size host
+    // chunks on this thread's stack; each chunk goes to the device array with
+    // one cudaMemcpyAsync from pageable memory, which returns once the bytes
+    // are staged, so the stack buffer can be reused at once.
+    thread_local Layout L;
+    constexpr int64_t kChunk = 32;
+    DecodeArgs chunk[kChunk];
+    int64_t units[kChunk + 1];
+    int64_t unit_total = 0;
+    int kind = -1, n_ctx = 0;
+    for (int64_t base = 0; base < n_items; base += kChunk) {
+        const int64_t n = std::min<int64_t>(kChunk, n_items - base);
+        for (int64_t i = 0; i < n; i++) {
+            const ep_batch_item& it = items[base + i];
+            st = fill_args(it.h_blob, it.d_blob, it.bytes, it.d_out, it.d_row_scale_out, nullptr, nullptr, L,
+                           &chunk[i]);
+            if (st != EP_OK) return st;
+            const int k = kind_of(L);
+            if (kind >= 0 && k != kind) return EP_ERR_INVALID_ARG;  // one container/mode per batch
+            kind = k;
+            n_ctx = std::max(n_ctx, L.n_ctx);
+            units[i] = unit_total;
+            const int64_t groups = (L.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
+            unit_total += (groups + kWarpsPerCta - 1) / kWarpsPerCta;
+        }
+        if (cudaMemcpyAsync(ws + sizeof(DecodeArgs) * (size_t)base, chunk, sizeof(DecodeArgs) * (size_t)n,
+                            cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(ws + units_off + sizeof(int64_t) * (size_t)base, units, sizeof(int64_t) * (size_t)n,
+                            cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return EP_ERR_CUDA;
+    }
+    units[0] = unit_total;  // unit_start[n_items]
+    if (cudaMemcpyAsync(ws + units_off + sizeof(int64_t) * (size_t)n_items, units, sizeof(int64_t),
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return EP_ERR_CUDA;
+    // the counters start at zero on every call; the previous call's values stay behind otherwise
+    if (cudaMemsetAsync(ws + ctr_off, 0, sizeof(BatchCounters) + sizeof(uint32_t) * (size_t)n_items, s) !=
+            cudaSuccess ||
+        cudaMemsetAsync(d_status, 0, sizeof(uint32_t), s) != cudaSuccess)
+        return EP_ERR_CUDA;
+    ep_batch_plan plan;
+    std::memset(&plan, 0, sizeof(plan));
+    plan.n_items = n_items;
+    plan.total_units = unit_total;
+    plan.ring = ring;
+    plan.kind = kind;
+    plan.n_ctx = n_ctx;
+    plan.d_workspace = ws;
+    plan.workspace_bytes = kStaticScratchBytes;
+    plan.items_off = 0;
+    plan.units_off = units_off;
+    plan.counters_off = ctr_off;
+    switch (kind) {
+        case K_BF16: return launch_batch<K_BF16>(&plan, d_status, s);
+        case K_FP16: return launch_batch<K_FP16>(&plan, d_status, s);
+        case K_FP8: return launch_batch<K_FP8>(&plan, d_status, s);
+        case K_INT8: return launch_batch<K_INT8>(&plan, d_status, s);
+        case K_LOSSLESS: return launch_batch<K_LOSSLESS>(&plan, d_status, s);
+    }
+    return EP_ERR_INVALID_ARG;
+}

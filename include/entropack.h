@@ -209,6 +209,34 @@ ep_status ep_compressed_linear(const uint8_t *h_blob, const void *d_blob, size_t
                                int64_t tokens, uint16_t *d_y, int32_t mode, void *d_ws, size_t ws_bytes,
                                uint32_t *d_status, ep_stream_t stream);
 
+/*
+ * Allocation-free variant of ep_batch_prepare + ep_batch_decode.  The pages
+ * have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory, such as code running under another framework's
+ * caching allocator or memory budget, plug-ins inside a host process that
+ * owns every allocation, and latency-critical paths where cudaMalloc would
+ * synchronise the device.  The batch kernel's scratch (item descriptors, unit
+ * table, claim and completion counters) lives in a device array inside the
+ * library, sized for EP_BATCH_STATIC_MAX_ITEMS streams (about 177 KB, held
+ * on every GPU that loads the library until the process exits).  The caller
+ * still passes the streams, the outputs and the status word, exactly as for
+ * ep_batch_prepare; ring has the same meaning.
+ *  - n_items > EP_BATCH_STATIC_MAX_ITEMS returns EP_ERR_INVALID_ARG before
+ *    any work is enqueued; so do the validation errors of ep_batch_prepare.
+ *  - No cudaMalloc, cudaFree or other allocating routine is called.  The
+ *    descriptors are copied to the device array from host stack memory with
+ *    cudaMemcpyAsync on `stream`; for pageable memory that copy may wait for
+ *    the stream's earlier work.  The counters are cleared on every call.
+ *  - The first call on a device looks up the array's device address with
+ *    cudaGetSymbolAddress (with that device current) and caches it; make that
+ *    first call before any stream capture.
+ *  - Every call shares the one array: calls whose work overlaps on the GPU
+ *    (for example on two streams) race and must be serialised by the caller.
+ */
+#define EP_BATCH_STATIC_MAX_ITEMS 1024
+ep_status ep_batch_decode_static(const ep_batch_item *items, int64_t n_items, int32_t ring, uint32_t *d_status,
+                                 ep_stream_t stream);
+
 /* Synchronise `stream` and map the status word: 0 -> EP_OK, any bit -> EP_ERR_CORRUPT. */
 ep_status ep_sync_status(const uint32_t *d_status, ep_stream_t stream);
 
