@@ -121,36 +121,86 @@ __device__ void build_tables(const DecodeArgs& a, uint32_t* tab, uint32_t* fr, u
 }
 
 // ---------------------------------------------------------------- rANS lane
-// State x in [2^16, 2^32) before every symbol; `next` is the word at index wi
-// of the lane's wn words (prefetched).  The refill is branch-free: the word
-// is spliced in with one byte permute and the prefetch of the following word
-// is predicated.  A corrupt lane never reads past its own words; it ends with
-// x != L or wi != wn and is reported.
+// State x in [2^16, 2^32) before every symbol.  A lane's 16-bit words are
+// staged in a private 128-byte ring in shared memory (8 chunks of 16 bytes,
+// chunk c of the payload in slot c % 8), filled by cp.async at block
+// boundaries (top_up).  Every symbol reads the word at the lane's position
+// together with its slot-table entry, so the refill never waits on a load
+// issued for an earlier symbol: the warp's register scoreboard would
+// otherwise stall all 32 lanes on whichever lane refilled last.
+constexpr uint32_t kRingChunks = 8;
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t saddr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(saddr) : "memory");
+    return v;
+}
+
 struct Lane {
     uint32_t x;
-    uint32_t next;
-    uint32_t wi, wn;
-    const uint16_t* w;
+    uint32_t a, aend;       // payload byte offsets: next word, one past the lane's last word
+    uint32_t issued, clast;  // next chunk to stage, last chunk of the lane (chunk = 16 bytes)
+    uint32_t iss1, iss2;     // `issued` after the previous two top-ups
+    uint32_t ring;           // shared-window address of the lane's ring (128-byte aligned)
+    const uint8_t* pay;
 
-    __device__ __forceinline__ void refill() {
+    __device__ __forceinline__ void stage_chunk() {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ring + ((issued % kRingChunks) << 4)),
+                     "l"(pay + ((size_t)issued << 4))
+                     : "memory");
+        issued++;
+    }
+    // Start a lane at payload offset a0 with n words: stage its first chunks and wait for them.
+    __device__ __forceinline__ void start(uint32_t a0, uint32_t n) {
+        a = a0;
+        aend = a0 + 2u * n;
+        issued = a0 >> 4;
+        clast = n ? ((aend - 1u) >> 4) : issued - 1u;  // empty lane: clast + 1 == issued, nothing to stage
+        const uint32_t target = n ? min(issued + kRingChunks, clast + 1u) : issued;
+        while (issued < target) stage_chunk();
+        iss1 = iss2 = issued;
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    }
+    // Block boundary: keep chunks [cpos, cpos + 8) staged.  A block reads at
+    // most 25 words (9 symbols and 8 two-byte escapes), i.e. chunks up to
+    // cpos + 4; those are complete once every group but the last two is, unless
+    // one of them was staged by the last two top-ups (then wait for all).
+    __device__ __forceinline__ void top_up() {
+        const uint32_t cpos = a >> 4;
+        const uint32_t target = min(cpos + kRingChunks, clast + 1u);
+        if (issued < target) stage_chunk();
+        if (issued < target) stage_chunk();
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        const bool urgent = iss2 <= min(cpos + 4u, clast) && aend != a;
+        iss2 = iss1;
+        iss1 = issued;
+        if (__any_sync(0xffffffffu, urgent || issued < target)) {
+            while (issued < target) stage_chunk();
+            iss1 = iss2 = issued;
+            asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 2;" ::: "memory");
+        }
+    }
+    __device__ __forceinline__ void renorm(uint32_t w) {
         const bool p = x < kRansL;
-        const uint32_t xr = __byte_perm(next, x, 0x5410);  // (x << 16) | next
-        x = p ? xr : x;
-        wi += p ? 1u : 0u;
-        if (p && wi < wn) next = __ldg(w + wi);
+        x = p ? __byte_perm(w, x, 0x5410) : x;  // (x << 16) | w
+        a += p ? 2u : 0u;
     }
     // one table symbol; returns the slot entry
     __device__ __forceinline__ uint32_t sym(const uint32_t* tab) {
+        const uint32_t w = lds_u16(ring | (a & 126u));
         const uint32_t e = tab[x & (kProbScale - 1)];
         x = (e >> 20) * (x >> kProbBits) + (e & 0xFFFu);
-        refill();
+        renorm(w);
         return e;
     }
     // one uniform byte (f = 16, cum = 16 * byte)
     __device__ __forceinline__ uint32_t byte() {
+        const uint32_t w = lds_u16(ring | (a & 126u));
         const uint32_t slot = x & (kProbScale - 1);
         x = 16u * (x >> kProbBits) + (slot & 15u);
-        refill();
+        renorm(w);
         return slot >> 4;
     }
 };
@@ -212,7 +262,7 @@ __device__ __forceinline__ void dump_syms(uint8_t* sym_out, int64_t eoff, const 
 // dummy state and store nothing), so warp votes are always uniform.
 template <int KIND, bool DUMP>
 __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t* tab, int64_t grp,
-                                             uint32_t* status) {
+                                             uint32_t* status, uint32_t ring_addr) {
     const int lane = threadIdx.x & 31, l = lane & 3, tig = lane >> 2;
     const int64_t K = a.cols;
     constexpr uint32_t kHdr = (KIND == K_LOSSLESS ? kRawBytesPerTile : 0) + kTileHeaderBytes;
@@ -231,9 +281,9 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
     const uint8_t* th = tb + (KIND == K_LOSSLESS ? kRawBytesPerTile : 0);
     Lane ln;
     ln.x = kRansL;
-    ln.wi = 0;
-    ln.wn = 0;
-    ln.w = reinterpret_cast<const uint16_t*>(a.payload);
+    ln.pay = a.payload;
+    ln.ring = ring_addr;
+    uint32_t a0 = 0, nwl = 0;
     if (active) {
         const uint2 nwv = *reinterpret_cast<const uint2*>(th + 16);
         const uint32_t nw[4] = {nwv.x & 0xFFFFu, nwv.x >> 16, nwv.y & 0xFFFFu, nwv.y >> 16};
@@ -245,11 +295,11 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
             active = false;
         } else {
             ln.x = reinterpret_cast<const uint32_t*>(th)[l];
-            ln.w = reinterpret_cast<const uint16_t*>(th + kTileHeaderBytes) + before;
-            ln.wn = l == 0 ? nw[0] : (l == 1 ? nw[1] : (l == 2 ? nw[2] : nw[3]));
+            a0 = (uint32_t)(th + kTileHeaderBytes + 2u * before - a.payload);
+            nwl = l == 0 ? nw[0] : (l == 1 ? nw[1] : (l == 2 ? nw[2] : nw[3]));
         }
     }
-    ln.next = ln.wn > 0 ? __ldg(ln.w) : 0u;
+    ln.start(a0, nwl);
 
     const int64_t tr0 = (tile / a.tiles_per_row) * kTileRows;
     const int64_t tc0 = (tile % a.tiles_per_row) * kTileCols;
@@ -262,6 +312,7 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
     for (int slab = 0; slab < 8; slab++) {
         for (int m2 = 0; m2 < 16; m2++) {
             const int j = slab * 16 + m2;
+            ln.top_up();
             const int64_t row = row0 + 2 * m2;
             const int64_t eoff = base + (int64_t)(2 * m2) * K + 16 * slab;
             if (KIND == K_LOSSLESS) {
@@ -350,13 +401,27 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
             }
         }
     }
-    if (active && (ln.x != kRansL || ln.wi != ln.wn)) flag(status, EP_STATUS_LANE_END);
+    if (active && (ln.x != kRansL || ln.a != ln.aend)) flag(status, EP_STATUS_LANE_END);
     if (esc_bad) flag(status, EP_STATUS_ESCAPE);
 }
 
 __device__ __forceinline__ void copy_row_scales(const DecodeArgs& a, int64_t first, int64_t stride) {
     if (a.scale_out)
         for (int64_t r = first; r < a.rows; r += stride) a.scale_out[r] = a.t[r];
+}
+
+// Shared-memory layout of a decode CTA: n_ctx slot tables (16 KB each), the
+// n_ctx x 256 frequency and cumulative-frequency scratch of the table build,
+// then one 128-byte word ring per thread (128-byte aligned; 128 bytes slack).
+constexpr size_t kRingBytes = (size_t)kThreads * 128 + 128;
+
+__host__ __device__ constexpr size_t decode_smem_bytes(int n_ctx) {
+    return (size_t)n_ctx * (kSlots + 512) * 4 + kRingBytes;
+}
+
+__device__ __forceinline__ uint32_t lane_ring(uint32_t* smem, int n_ctx) {
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem + n_ctx * (kSlots + 512));
+    return ((base + 127u) & ~127u) + 128u * threadIdx.x;
 }
 
 // ------------------------------------------------------------ single stream
@@ -374,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     const int64_t n_groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
     const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta;
     for (int64_t grp = (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x; grp < n_groups; grp += stride)
-        decode_group<KIND, DUMP>(a, tab, grp, a.status);
+        decode_group<KIND, DUMP>(a, tab, grp, a.status, lane_ring(smem, a.n_ctx));
 }
 
 // ----------------------------------------------------------------- batched
@@ -441,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int64_t grp = (unit - unit_start[item]) * kWarpsPerCta + (threadIdx.x >> 5);
         const int64_t n_groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
-        if (!s_skip && grp < n_groups) decode_group<KIND, false>(a, tab, grp, status);
+        if (!s_skip && grp < n_groups) decode_group<KIND, false>(a, tab, grp, status, lane_ring(smem, kLossyContexts));
         if ((KIND == K_FP8 || KIND == K_INT8) && unit == unit_start[item])
             copy_row_scales(a, threadIdx.x, blockDim.x);
         __syncthreads();
@@ -453,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------ launching
-constexpr size_t kMaxSmem = (size_t)ep::kLossyContexts * (kSlots + 512) * 4;
+constexpr size_t kMaxSmem = decode_smem_bytes(kLossyContexts);
 
 struct DeviceInfo {
     int sms = 0;
@@ -541,7 +606,7 @@ ep_status launch_batch(const ep_batch_plan* p, uint32_t* d_status, cudaStream_t 
     });
     if (attr_err != cudaSuccess) return EP_ERR_CUDA;
     uint8_t* ws = static_cast<uint8_t*>(p->d_workspace);
-    const size_t smem = (size_t)p->n_ctx * (kSlots + 512) * 4;
+    const size_t smem = decode_smem_bytes(kLossyContexts);
     const int64_t cap = device_info().sms;
     const int grid = (int)(p->total_units < cap ? p->total_units : cap);
     if (grid <= 0) return EP_OK;
@@ -559,7 +624,7 @@ ep_status decode_impl(const uint8_t* h_blob, const void* d_blob, size_t bytes, v
     ep_status st = fill_args(h_blob, d_blob, bytes, d_out, d_scale, d_sym, d_status, L, &a);
     if (st != EP_OK) return st;
     if (cudaMemsetAsync(d_status, 0, sizeof(uint32_t), stream) != cudaSuccess) return EP_ERR_CUDA;
-    const size_t smem = (size_t)L.n_ctx * (kSlots + 512) * 4;
+    const size_t smem = decode_smem_bytes(L.n_ctx);
     const bool dump = d_sym != nullptr;
     switch (kind_of(L)) {
         case K_BF16: return dump ? launch<K_BF16, true>(a, smem, stream) : launch<K_BF16, false>(a, smem, stream);
