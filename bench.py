@@ -55,60 +55,98 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """SM clocks and clock-event (throttle) reasons sampled during the timed region.
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    Reads NVML every 5 ms from a background thread (read-only queries; no
+    setting of the GPU is touched).  Falls back to `nvidia-smi -lms 50` when
+    the NVML binding is missing.
+    """
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40), ("sw_thermal_slowdown", 0x20),
+               ("sw_power_cap", 0x4), ("hw_power_brake_slowdown", 0x80))
+
+    def __init__(self, cuda_index: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v for v in vis.split(",") if v.strip()]
+        self.gpu = int(ids[cuda_index]) if ids and ids[cuda_index].strip().isdigit() else cuda_index
+        self.samples, self.max_mhz, self.stop = [], None, threading.Event()
+        self.thread = None
         self.proc = None
-        self.lines = []
-        self.reader = None
+
+    def _nvml_loop(self, pynvml, h):
+        while not self.stop.is_set():
+            try:
+                sm = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
+                rs = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
+                self.samples.append((float(sm), int(rs)))
+            except Exception:
+                pass
+            self.stop.wait(0.005)
+
+    def _smi_loop(self):
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={q}",
+                                      "--format=csv,noheader,nounits", "-lms", "50"],
+                                     stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        bits = [0x8, 0x40, 0x20, 0x4]
+        for line in self.proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            try:
+                self.max_mhz = float(f[1])
+                rs = sum(b for b, v in zip(bits, f[2:6]) if v.lower() == "active")
+                self.samples.append((float(f[0]), rs))
+            except (ValueError, IndexError):
+                continue
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.reader = threading.Thread(target=self._read, daemon=True)
-            self.reader.start()
-        except (OSError, FileNotFoundError):
-            self.proc = None
+            import pynvml
+            pynvml.nvmlInit()
+            h = pynvml.nvmlDeviceGetHandleByIndex(self.gpu)
+            self.max_mhz = float(pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM))
+            self.thread = threading.Thread(target=self._nvml_loop, args=(pynvml, h), daemon=True)
+        except Exception:
+            self.thread = threading.Thread(target=self._smi_loop, daemon=True)
+        self.thread.start()
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
+        self.stop.set()
         if self.proc is not None:
             self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
         return False
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        sm.sort()
-        med = sm[len(sm) // 2] if sm else None
-        return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        sm = sorted(v for v, _ in self.samples)
+        reasons = sorted({n for _, r in self.samples for n, b in self.REASONS if r & b})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(sm)}
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over all ranks (the slowest rank's time); x itself on one process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, steps: int, world: int, elapsed_s: float) -> float:
+    """Whole-job rate: the units every rank processed (replicas: each decodes the whole model)
+    over the slowest rank's time."""
+    return units_per_rank * steps * world / elapsed_s
 
 
 def source_sha() -> str:
@@ -173,8 +211,7 @@ def run_ours(args, rank, world, device):
     ep.sync_status(bd.status, stream)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     torch.cuda.synchronize(device)
     with ClockSampler(torch.cuda.current_device()) as clk:
         t_start = time.perf_counter()
@@ -184,15 +221,12 @@ def run_ours(args, rank, world, device):
             ev[i][1].record(stream)
         torch.cuda.synchronize(device)
         wall = time.perf_counter() - t_start
+    barrier(world)
     ep.sync_status(bd.status, stream)
     per_launch_ms = [a.elapsed_time(b) for a, b in ev]
     step_ms = sum(per_launch_ms) / len(per_launch_ms)
-    elapsed = sum(per_launch_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed = float(t.item())
-    value = n_params * args.steps * world / elapsed / 1e9
+    elapsed = max_over_ranks(sum(per_launch_ms) / 1e3, device)
+    value = job_throughput(n_params, args.steps, world, elapsed) / 1e9
     alg_bytes = comp_bytes + 2 * n_params  # compressed read + BF16 written
     achieved_gbs = alg_bytes / (step_ms / 1e3) / 1e9
 
@@ -377,7 +411,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--blocks", type=int, default=30)
