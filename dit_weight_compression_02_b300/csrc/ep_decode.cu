@@ -130,19 +130,20 @@ __device__ void build_tables(const DecodeArgs& a, uint32_t* tab, uint32_t* fr, u
 // otherwise stall all 32 lanes on whichever lane refilled last.
 constexpr uint32_t kRingChunks = 8;
 
-__device__ __forceinline__ uint32_t lds_u16(uint32_t saddr) {
-    uint16_t v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(saddr) : "memory");
-    return v;
-}
+extern __shared__ __align__(128) uint32_t g_smem[];  // the decode CTA's dynamic shared memory
 
 struct Lane {
-    uint32_t x;
+    uint32_t x, next;
     uint32_t a, aend;       // payload byte offsets: next word, one past the lane's last word
     uint32_t issued, clast;  // next chunk to stage, last chunk of the lane (chunk = 16 bytes)
-    uint32_t iss1, iss2;     // `issued` after the previous two top-ups
-    uint32_t ring;           // shared-window address of the lane's ring (128-byte aligned)
+    uint32_t roff;           // byte offset of the lane's 128-byte ring in g_smem (a multiple of 128)
+    uint32_t ring;           // shared-window address of the same ring (for cp.async)
     const uint8_t* pay;
+
+    // the 16-bit word at payload offset o (even): slot (o / 16) % 8 of the ring
+    __device__ __forceinline__ uint32_t word_at(uint32_t o) const {
+        return reinterpret_cast<const uint16_t*>(g_smem)[(roff | (o & 126u)) >> 1];
+    }
 
     __device__ __forceinline__ void stage_chunk() {
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ring + ((issued % kRingChunks) << 4)),
@@ -158,49 +159,51 @@ struct Lane {
         clast = n ? ((aend - 1u) >> 4) : issued - 1u;  // empty lane: clast + 1 == issued, nothing to stage
         const uint32_t target = n ? min(issued + kRingChunks, clast + 1u) : issued;
         while (issued < target) stage_chunk();
-        iss1 = iss2 = issued;
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        next = word_at(a);
     }
-    // Block boundary: keep chunks [cpos, cpos + 8) staged.  A block reads at
-    // most 25 words (9 symbols and 8 two-byte escapes), i.e. chunks up to
-    // cpos + 4; those are complete once every group but the last two is, unless
-    // one of them was staged by the last two top-ups (then wait for all).
+    // Block boundary.  Each top-up commits one group holding at most one
+    // chunk, so chunk c < issued was staged at least issued - 1 - c top-ups
+    // ago.  A block reads at most 9 words plus, on the escape path, 16 more
+    // (chunks up to cpos + 4); when chunk min(cpos + 4, clast) is at least three
+    // top-ups old, waiting for every group but the newest three suffices.
+    // Otherwise (ring behind after a burst, or a short lane) stage all and wait.
     __device__ __forceinline__ void top_up() {
         const uint32_t cpos = a >> 4;
         const uint32_t target = min(cpos + kRingChunks, clast + 1u);
         if (issued < target) stage_chunk();
-        if (issued < target) stage_chunk();
         asm volatile("cp.async.commit_group;" ::: "memory");
-        const bool urgent = iss2 <= min(cpos + 4u, clast) && aend != a;
-        iss2 = iss1;
-        iss1 = issued;
-        if (__any_sync(0xffffffffu, urgent || issued < target)) {
+        const uint32_t need = min(cpos + 4u, clast);
+        const bool urgent = a != aend && (int32_t)(issued - 1u - need) < 3;
+        if (__any_sync(0xffffffffu, urgent)) {
             while (issued < target) stage_chunk();
-            iss1 = iss2 = issued;
             asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
         } else {
-            asm volatile("cp.async.wait_group 2;" ::: "memory");
+            asm volatile("cp.async.wait_group 3;" ::: "memory");
         }
     }
-    __device__ __forceinline__ void renorm(uint32_t w) {
-        const bool p = x < kRansL;
-        x = p ? __byte_perm(w, x, 0x5410) : x;  // (x << 16) | w
-        a += p ? 2u : 0u;
+    // x < 2^16: shift in the prefetched word, then read the following one.  Only
+    // lanes that refilled touch shared memory; the new word is first used one
+    // symbol later, by which time the load has landed.
+    __device__ __forceinline__ void renorm() {
+        if (x < kRansL) {
+            x = (x << 16) | next;
+            a += 2u;
+            next = word_at(a);
+        }
     }
     // one table symbol; returns the slot entry
     __device__ __forceinline__ uint32_t sym(const uint32_t* tab) {
-        const uint32_t w = lds_u16(ring | (a & 126u));
         const uint32_t e = tab[x & (kProbScale - 1)];
         x = (e >> 20) * (x >> kProbBits) + (e & 0xFFFu);
-        renorm(w);
+        renorm();
         return e;
     }
     // one uniform byte (f = 16, cum = 16 * byte)
     __device__ __forceinline__ uint32_t byte() {
-        const uint32_t w = lds_u16(ring | (a & 126u));
         const uint32_t slot = x & (kProbScale - 1);
         x = 16u * (x >> kProbBits) + (slot & 15u);
-        renorm(w);
+        renorm();
         return slot >> 4;
     }
 };
@@ -262,9 +265,15 @@ __device__ __forceinline__ void dump_syms(uint8_t* sym_out, int64_t eoff, const 
 // dummy state and store nothing), so warp votes are always uniform.
 template <int KIND, bool DUMP>
 __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t* tab, int64_t grp,
-                                             uint32_t* status, uint32_t ring_addr) {
+                                             uint32_t* status, uint32_t ring_off) {
     const int lane = threadIdx.x & 31, l = lane & 3, tig = lane >> 2;
     const int64_t K = a.cols;
+    // fields used inside the block loop, read once: the batched kernel's
+    // descriptors live in global memory, which the output stores could alias
+    const float* const gp = a.g;
+    const float* const mp = a.m;
+    void* const outp = a.out;
+    uint8_t* const symp = a.sym_out;
     constexpr uint32_t kHdr = (KIND == K_LOSSLESS ? kRawBytesPerTile : 0) + kTileHeaderBytes;
     const int64_t tile = grp * kTilesPerWarp + tig;
     bool active = tile < a.n_tiles;
@@ -282,7 +291,8 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
     Lane ln;
     ln.x = kRansL;
     ln.pay = a.payload;
-    ln.ring = ring_addr;
+    ln.roff = ring_off;
+    ln.ring = (uint32_t)__cvta_generic_to_shared(g_smem) + ring_off;
     uint32_t a0 = 0, nwl = 0;
     if (active) {
         const uint2 nwv = *reinterpret_cast<const uint2*>(th + 16);
@@ -308,13 +318,19 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
     const int64_t row0 = tr0 + (l >> 1);
     const int64_t base = row0 * K + tc0 + 8 * (l & 1);
     bool esc_bad = false;
+    // the lane's 16 rows: g at gr[2 m2], m at mr[2 m2]; output element offset of
+    // block (slab, m2) is base + 16 slab + 2 m2 K, advanced with running offsets
+    const float* const gr = gp + row0;
+    const float* const mr = mp + row0;
+    const int64_t step = 2 * K;
+    float gnext = active ? __ldg(gr) : 0.f;
 
     for (int slab = 0; slab < 8; slab++) {
-        for (int m2 = 0; m2 < 16; m2++) {
+        int64_t eoff = base + 16 * slab;
+#pragma unroll 2
+        for (int m2 = 0; m2 < 16; m2++, eoff += step) {
             const int j = slab * 16 + m2;
             ln.top_up();
-            const int64_t row = row0 + 2 * m2;
-            const int64_t eoff = base + (int64_t)(2 * m2) * K + 16 * slab;
             if (KIND == K_LOSSLESS) {
                 uint2 raw = make_uint2(0, 0);
                 if (active) raw = *reinterpret_cast<const uint2*>(tb + 8 * (4 * j + l));
@@ -331,20 +347,21 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
                     w[h] = v0 | (v1 << 16);
                 }
                 if (active) {
-                    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + eoff) =
+                    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(outp) + eoff) =
                         make_uint4(w[0], w[1], w[2], w[3]);
                     if (DUMP) {
                         uint32_t u[8];
 #pragma unroll
                         for (int i = 0; i < 8; i++) u[i] = sym_byte(e[i]);
-                        dump_syms(a.sym_out, eoff, u);
+                        dump_syms(symp, eoff, u);
                     }
                 }
                 continue;
             }
-            const float g = active ? __ldg(a.g + row) : 0.f;
+            const float g = gnext;  // prefetched one block ahead (the L1 beside the rings is small)
+            gnext = (active && j + 1 < kBlocksPerLane) ? __ldg(gr + 2 * ((m2 + 1) & 15)) : 0.f;
             float mult = g;
-            if (KIND == K_FP8 || KIND == K_INT8) mult = active ? __ldg(a.m + row) : 0.f;
+            if (KIND == K_FP8 || KIND == K_INT8) mult = active ? __ldg(mr + 2 * m2) : 0.f;
             uint32_t e[8];
             e[0] = ln.sym(tab);
             const uint32_t* t1 = tab + kSlots + ((e[0] >> 12) & 1u) * kSlots;  // context 1 + c
@@ -391,12 +408,12 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
                 for (int i = 0; i < 8; i++) y[i] = fmaf(__uint_as_float(F[i]), mult, cst);
             }
             if (active) {
-                store_block<KIND>(a.out, eoff, y);
+                store_block<KIND>(outp, eoff, y);
                 if (DUMP) {
                     uint32_t u[8];
 #pragma unroll
                     for (int i = 0; i < 8; i++) u[i] = sym_byte(e[i]);
-                    dump_syms(a.sym_out, eoff, u);
+                    dump_syms(symp, eoff, u);
                 }
             }
         }
@@ -410,18 +427,19 @@ __device__ __forceinline__ void copy_row_scales(const DecodeArgs& a, int64_t fir
         for (int64_t r = first; r < a.rows; r += stride) a.scale_out[r] = a.t[r];
 }
 
-// Shared-memory layout of a decode CTA: n_ctx slot tables (16 KB each), the
-// n_ctx x 256 frequency and cumulative-frequency scratch of the table build,
-// then one 128-byte word ring per thread (128-byte aligned; 128 bytes slack).
-constexpr size_t kRingBytes = (size_t)kThreads * 128 + 128;
+// Shared-memory layout of a decode CTA (g_smem, 128-byte aligned): n_ctx slot
+// tables (16 KB each), the n_ctx x 256 frequency and cumulative-frequency
+// scratch of the table build, then one 128-byte word ring per thread.
+constexpr size_t kRingBytes = (size_t)kThreads * 128;
 
 __host__ __device__ constexpr size_t decode_smem_bytes(int n_ctx) {
     return (size_t)n_ctx * (kSlots + 512) * 4 + kRingBytes;
 }
 
-__device__ __forceinline__ uint32_t lane_ring(uint32_t* smem, int n_ctx) {
-    const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem + n_ctx * (kSlots + 512));
-    return ((base + 127u) & ~127u) + 128u * threadIdx.x;
+// byte offset of this thread's ring in g_smem: after the tables and their
+// build scratch of n_ctx contexts (18432 bytes each, a multiple of 128)
+__device__ __forceinline__ uint32_t lane_ring(int n_ctx) {
+    return (uint32_t)n_ctx * (kSlots + 512) * 4 + 128u * threadIdx.x;
 }
 
 // ------------------------------------------------------------ single stream
@@ -429,7 +447,7 @@ __device__ __forceinline__ uint32_t lane_ring(uint32_t* smem, int n_ctx) {
 // g % gridDim.x), so a small matrix still spreads over every SM.
 template <int KIND, bool DUMP>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a) {
-    extern __shared__ uint32_t smem[];
+    uint32_t* const smem = g_smem;
     uint32_t* tab = smem;                    // n_ctx x 4096
     uint32_t* fr = smem + a.n_ctx * kSlots;  // n_ctx x 256
     uint32_t* cu = fr + a.n_ctx * 256;       // n_ctx x 256
@@ -439,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     const int64_t n_groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
     const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta;
     for (int64_t grp = (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x; grp < n_groups; grp += stride)
-        decode_group<KIND, DUMP>(a, tab, grp, a.status, lane_ring(smem, a.n_ctx));
+        decode_group<KIND, DUMP>(a, tab, grp, a.status, lane_ring(a.n_ctx));
 }
 
 // ----------------------------------------------------------------- batched
@@ -463,7 +481,7 @@ template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     batch_kernel(const DecodeArgs* __restrict__ items, const int64_t* __restrict__ unit_start, int64_t n_items,
                  int32_t ring, BatchCounters* ctr, uint32_t* status) {
-    extern __shared__ uint32_t smem[];
+    uint32_t* const smem = g_smem;
     __shared__ int64_t s_unit, s_item;
     __shared__ int s_skip;
     uint32_t* done = reinterpret_cast<uint32_t*>(ctr + 1);
@@ -506,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int64_t grp = (unit - unit_start[item]) * kWarpsPerCta + (threadIdx.x >> 5);
         const int64_t n_groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
-        if (!s_skip && grp < n_groups) decode_group<KIND, false>(a, tab, grp, status, lane_ring(smem, kLossyContexts));
+        if (!s_skip && grp < n_groups) decode_group<KIND, false>(a, tab, grp, status, lane_ring(kLossyContexts));
         if ((KIND == K_FP8 || KIND == K_INT8) && unit == unit_start[item])
             copy_row_scales(a, threadIdx.x, blockDim.x);
         __syncthreads();

@@ -137,7 +137,8 @@ ep_status ep_decode_symbols(const uint8_t *h_blob, const void *d_blob, size_t by
 /*
  * Batched decode: many streams (e.g. every linear layer of a model) in one
  * persistent launch.  All items must share mode and container.  Work is cut
- * into units of 128 tiles of one stream; CTAs claim units in item order.
+ * into units of 32 groups of 8 tiles (256 tiles) of one item; CTAs (one per
+ * SM) claim units in item order, one warp per group.
  *
  *   ring == 0  every item writes its own d_out (outputs must not overlap);
  *   ring == R  item i may reuse the output buffer of item i - R ("decode back
@@ -164,7 +165,7 @@ typedef struct {
 } ep_batch_item;
 
 typedef struct {
-    int64_t n_items, total_units;
+    int64_t n_items, total_units; /* total_units: work units (32 tile groups) of all items */
     int32_t ring, kind, n_ctx, reserved;
     void *d_workspace;
     size_t workspace_bytes;
