@@ -419,7 +419,7 @@ def main():
     ap.add_argument("--target-bpp", type=float, default=4.0)
     ap.add_argument("--no-linear", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--cpu-sample-layers", type=int, default=21)
+    ap.add_argument("--cpu-sample-layers", type=int, default=210)
     ap.add_argument("--ref-layers", type=int, default=7)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup

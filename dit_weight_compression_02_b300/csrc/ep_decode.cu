@@ -39,7 +39,6 @@ namespace ep {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kWarpsPerCta = kThreads / 32;
 constexpr int kTilesPerWarp = 8;
 constexpr int kSlots = 4096;
 constexpr uint32_t kMagicLo = 0x44C00000u;  // 1536.0f: bits 12..19 carry u, worth u/2
@@ -162,25 +161,24 @@ struct Lane {
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
         next = word_at(a);
     }
-    // Block boundary.  Each top-up commits one group holding at most one
-    // chunk, so chunk c < issued was staged at least issued - 1 - c top-ups
-    // ago.  A block reads at most 9 words plus, on the escape path, 16 more
-    // (chunks up to cpos + 4); when chunk min(cpos + 4, clast) is at least three
-    // top-ups old, waiting for every group but the newest three suffices.
-    // Otherwise (ring behind after a burst, or a short lane) stage all and wait.
-    __device__ __forceinline__ void top_up() {
+    // Block boundary (see top_up below): stage at most one chunk for this lane
+    // and report whether the block's reads are not yet known to be complete.
+    // Each block commits one cp.async group per thread, so chunk c < issued
+    // was staged at least issued - 1 - c blocks ago.  A block reads at most 9
+    // words plus, on the escape path, 16 more (chunks up to cpos + 4); when
+    // chunk min(cpos + 4, clast) is at least three blocks old, waiting for
+    // every group but the newest three suffices.
+    __device__ __forceinline__ bool stage_step() {
         const uint32_t cpos = a >> 4;
         const uint32_t target = min(cpos + kRingChunks, clast + 1u);
         if (issued < target) stage_chunk();
-        asm volatile("cp.async.commit_group;" ::: "memory");
         const uint32_t need = min(cpos + 4u, clast);
-        const bool urgent = a != aend && (int32_t)(issued - 1u - need) < 3;
-        if (__any_sync(0xffffffffu, urgent)) {
-            while (issued < target) stage_chunk();
-            asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-        } else {
-            asm volatile("cp.async.wait_group 3;" ::: "memory");
-        }
+        return a != aend && (int32_t)(issued - 1u - need) < 3;
+    }
+    // slow path: stage everything the ring can hold (the caller then waits for all)
+    __device__ __forceinline__ void stage_all() {
+        const uint32_t target = min((a >> 4) + kRingChunks, clast + 1u);
+        while (issued < target) stage_chunk();
     }
     // x < 2^16: shift in the prefetched word, then read the following one.  Only
     // lanes that refilled touch shared memory; the new word is first used one
@@ -207,6 +205,25 @@ struct Lane {
         return slot >> 4;
     }
 };
+
+// Block-boundary top-up of the NL lanes a thread decodes: one cp.async group
+// per block; if any lane of the warp might read a chunk that is not known to
+// be complete, stage all and wait for everything (rare: bursts of escapes,
+// short lanes), otherwise wait only for groups at least three blocks old.
+template <int NL>
+__device__ __forceinline__ void top_up(Lane (&ln)[NL]) {
+    bool urgent = false;
+#pragma unroll
+    for (int i = 0; i < NL; i++) urgent |= ln[i].stage_step();
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    if (__any_sync(0xffffffffu, urgent)) {
+#pragma unroll
+        for (int i = 0; i < NL; i++) ln[i].stage_all();
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    } else {
+        asm volatile("cp.async.wait_group 3;" ::: "memory");
+    }
+}
 
 __device__ __forceinline__ void flag(uint32_t* status, uint32_t bits) { atomicOr(status, bits); }
 
@@ -260,166 +277,217 @@ __device__ __forceinline__ void dump_syms(uint8_t* sym_out, int64_t eoff, const 
 }
 
 // ------------------------------------------------------------- one group
-// One warp decodes tile group `grp` (8 tiles, one rANS lane per thread).
-// Every lane runs the same number of steps (inactive lanes decode from a
-// dummy state and store nothing), so warp votes are always uniform.
-template <int KIND, bool DUMP>
-__device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t* tab, int64_t grp,
+// A warp decodes NL tile groups at once: thread (tig, l) runs rANS lane l of
+// tile tig of each group, interleaving the NL independent lanes so that one
+// lane's table-load latency overlaps the other's arithmetic.  Every thread
+// runs the same number of steps (inactive lanes decode from a dummy state and
+// store nothing), so warp votes are always uniform.
+template <int KIND>
+struct LaneTile {
+    bool active;
+    const uint8_t* tb;  // tile payload (lossless: raw bytes first)
+    int64_t base;       // output element offset of the lane's block (slab 0, m2 0)
+    const float* gr;    // row steps of the lane's rows: gr[2 m2]
+    const float* mr;    // FP8/INT8 multipliers: mr[2 m2]
+    float gnext;        // row step of the next block (prefetched one block ahead)
+
+    // validate the tile, find the lane's words and start the lane
+    __device__ __forceinline__ void setup(const DecodeArgs& a, int64_t grp, Lane& ln, uint32_t ring_off,
+                                          uint32_t* status) {
+        const int lane = threadIdx.x & 31, l = lane & 3, tig = lane >> 2;
+        constexpr uint32_t kHdr = (KIND == K_LOSSLESS ? kRawBytesPerTile : 0) + kTileHeaderBytes;
+        const int64_t tile = grp * kTilesPerWarp + tig;
+        active = grp >= 0 && tile < a.n_tiles;
+        uint64_t o0 = 0, o1 = 0;
+        if (active) {
+            o0 = a.tile_off[tile];
+            o1 = a.tile_off[tile + 1];
+            if (o0 > o1 || o1 > a.payload_bytes || (o0 & 15u) || o1 - o0 < kHdr) {
+                if (l == 0) flag(status, EP_STATUS_TILE_BOUNDS);
+                active = false;
+            }
+        }
+        tb = a.payload + (active ? o0 : 0);
+        const uint8_t* th = tb + (KIND == K_LOSSLESS ? kRawBytesPerTile : 0);
+        ln.x = kRansL;
+        ln.pay = a.payload;
+        ln.roff = ring_off;
+        ln.ring = (uint32_t)__cvta_generic_to_shared(g_smem) + ring_off;
+        uint32_t a0 = 0, nwl = 0;
+        if (active) {
+            const uint2 nwv = *reinterpret_cast<const uint2*>(th + 16);
+            const uint32_t nw[4] = {nwv.x & 0xFFFFu, nwv.x >> 16, nwv.y & 0xFFFFu, nwv.y >> 16};
+            const uint32_t total = nw[0] + nw[1] + nw[2] + nw[3];
+            uint32_t before = 0;
+            for (int i = 0; i < 4; i++) before += (i < l) ? nw[i] : 0u;
+            if (kHdr + 2ull * total > o1 - o0) {
+                if (l == 0) flag(status, EP_STATUS_TILE_BOUNDS);
+                active = false;
+            } else {
+                ln.x = reinterpret_cast<const uint32_t*>(th)[l];
+                a0 = (uint32_t)(th + kTileHeaderBytes + 2u * before - a.payload);
+                nwl = l == 0 ? nw[0] : (l == 1 ? nw[1] : (l == 2 ? nw[2] : nw[3]));
+            }
+        }
+        ln.start(a0, nwl);
+        const int64_t t = active ? tile : 0;
+        const int64_t tr0 = (t / a.tiles_per_row) * kTileRows;
+        const int64_t tc0 = (t % a.tiles_per_row) * kTileCols;
+        // this lane's block of step j sits at tile row 2 (j % 16) + l / 2 and
+        // tile column 16 (j / 16) + 8 (l % 2)
+        const int64_t row0 = tr0 + (l >> 1);
+        base = row0 * a.cols + tc0 + 8 * (l & 1);
+        gr = a.g + row0;
+        mr = a.m + row0;
+        gnext = active ? __ldg(gr) : 0.f;
+    }
+};
+
+template <int KIND, bool DUMP, int NL>
+__device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t* tab, int64_t grp0,
                                              uint32_t* status, uint32_t ring_off) {
-    const int lane = threadIdx.x & 31, l = lane & 3, tig = lane >> 2;
-    const int64_t K = a.cols;
     // fields used inside the block loop, read once: the batched kernel's
     // descriptors live in global memory, which the output stores could alias
-    const float* const gp = a.g;
-    const float* const mp = a.m;
     void* const outp = a.out;
     uint8_t* const symp = a.sym_out;
-    constexpr uint32_t kHdr = (KIND == K_LOSSLESS ? kRawBytesPerTile : 0) + kTileHeaderBytes;
-    const int64_t tile = grp * kTilesPerWarp + tig;
-    bool active = tile < a.n_tiles;
-    uint64_t o0 = 0, o1 = 0;
-    if (active) {
-        o0 = a.tile_off[tile];
-        o1 = a.tile_off[tile + 1];
-        if (o0 > o1 || o1 > a.payload_bytes || (o0 & 15u) || o1 - o0 < kHdr) {
-            if (l == 0) flag(status, EP_STATUS_TILE_BOUNDS);
-            active = false;
-        }
+    const int64_t step = 2 * a.cols;
+    const int l = threadIdx.x & 3;
+    Lane ln[NL];
+    LaneTile<KIND> T[NL];
+    bool esc_bad[NL];
+#pragma unroll
+    for (int i = 0; i < NL; i++) {
+        T[i].setup(a, grp0 + i, ln[i], ring_off + 128u * i, status);
+        esc_bad[i] = false;
     }
-    const uint8_t* tb = a.payload + (active ? o0 : 0);
-    const uint8_t* th = tb + (KIND == K_LOSSLESS ? kRawBytesPerTile : 0);
-    Lane ln;
-    ln.x = kRansL;
-    ln.pay = a.payload;
-    ln.roff = ring_off;
-    ln.ring = (uint32_t)__cvta_generic_to_shared(g_smem) + ring_off;
-    uint32_t a0 = 0, nwl = 0;
-    if (active) {
-        const uint2 nwv = *reinterpret_cast<const uint2*>(th + 16);
-        const uint32_t nw[4] = {nwv.x & 0xFFFFu, nwv.x >> 16, nwv.y & 0xFFFFu, nwv.y >> 16};
-        const uint32_t total = nw[0] + nw[1] + nw[2] + nw[3];
-        uint32_t before = 0;
-        for (int i = 0; i < 4; i++) before += (i < l) ? nw[i] : 0u;
-        if (kHdr + 2ull * total > o1 - o0) {
-            if (l == 0) flag(status, EP_STATUS_TILE_BOUNDS);
-            active = false;
-        } else {
-            ln.x = reinterpret_cast<const uint32_t*>(th)[l];
-            a0 = (uint32_t)(th + kTileHeaderBytes + 2u * before - a.payload);
-            nwl = l == 0 ? nw[0] : (l == 1 ? nw[1] : (l == 2 ? nw[2] : nw[3]));
-        }
-    }
-    ln.start(a0, nwl);
-
-    const int64_t tr0 = (tile / a.tiles_per_row) * kTileRows;
-    const int64_t tc0 = (tile % a.tiles_per_row) * kTileCols;
-    // this lane's block of step j sits at tile row 2 (j % 16) + l / 2 and
-    // tile column 16 (j / 16) + 8 (l % 2)
-    const int64_t row0 = tr0 + (l >> 1);
-    const int64_t base = row0 * K + tc0 + 8 * (l & 1);
-    bool esc_bad = false;
-    // the lane's 16 rows: g at gr[2 m2], m at mr[2 m2]; output element offset of
-    // block (slab, m2) is base + 16 slab + 2 m2 K, advanced with running offsets
-    const float* const gr = gp + row0;
-    const float* const mr = mp + row0;
-    const int64_t step = 2 * K;
-    float gnext = active ? __ldg(gr) : 0.f;
 
     for (int slab = 0; slab < 8; slab++) {
-        int64_t eoff = base + 16 * slab;
+        int64_t eoff[NL];
+#pragma unroll
+        for (int i = 0; i < NL; i++) eoff[i] = T[i].base + 16 * slab;
 #pragma unroll 2
-        for (int m2 = 0; m2 < 16; m2++, eoff += step) {
+        for (int m2 = 0; m2 < 16; m2++) {
             const int j = slab * 16 + m2;
-            ln.top_up();
-            if (KIND == K_LOSSLESS) {
-                uint2 raw = make_uint2(0, 0);
-                if (active) raw = *reinterpret_cast<const uint2*>(tb + 8 * (4 * j + l));
-                uint32_t e[8];
+            top_up<NL>(ln);
+            if constexpr (KIND == K_LOSSLESS) {
+                uint32_t e[NL][8];
 #pragma unroll
-                for (int i = 0; i < 8; i++) e[i] = ln.sym(tab);
-                uint32_t w[4];
+                for (int k = 0; k < 8; k++)
 #pragma unroll
-                for (int h = 0; h < 4; h++) {
-                    const uint32_t rw = (h < 2 ? raw.x : raw.y) >> (16 * (h & 1));
-                    const uint32_t r0 = rw & 0xFFu, r1 = (rw >> 8) & 0xFFu;
-                    const uint32_t v0 = ((r0 & 0x80u) << 8) | ((e[2 * h] >> 5) & 0x7F80u) | (r0 & 0x7Fu);
-                    const uint32_t v1 = ((r1 & 0x80u) << 8) | ((e[2 * h + 1] >> 5) & 0x7F80u) | (r1 & 0x7Fu);
-                    w[h] = v0 | (v1 << 16);
+                    for (int i = 0; i < NL; i++) e[i][k] = ln[i].sym(tab);
+#pragma unroll
+                for (int i = 0; i < NL; i++) {
+                    uint2 raw = make_uint2(0, 0);
+                    if (T[i].active) raw = *reinterpret_cast<const uint2*>(T[i].tb + 8 * (4 * j + l));
+                    uint32_t w[4];
+#pragma unroll
+                    for (int h = 0; h < 4; h++) {
+                        const uint32_t rw = (h < 2 ? raw.x : raw.y) >> (16 * (h & 1));
+                        const uint32_t r0 = rw & 0xFFu, r1 = (rw >> 8) & 0xFFu;
+                        const uint32_t v0 = ((r0 & 0x80u) << 8) | ((e[i][2 * h] >> 5) & 0x7F80u) | (r0 & 0x7Fu);
+                        const uint32_t v1 = ((r1 & 0x80u) << 8) | ((e[i][2 * h + 1] >> 5) & 0x7F80u) | (r1 & 0x7Fu);
+                        w[h] = v0 | (v1 << 16);
+                    }
+                    if (T[i].active) {
+                        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(outp) + eoff[i]) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                        if (DUMP) {
+                            uint32_t u[8];
+#pragma unroll
+                            for (int k = 0; k < 8; k++) u[k] = sym_byte(e[i][k]);
+                            dump_syms(symp, eoff[i], u);
+                        }
+                    }
+                    eoff[i] += step;
                 }
-                if (active) {
-                    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(outp) + eoff) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+            float mult[NL];
+#pragma unroll
+            for (int i = 0; i < NL; i++) {
+                mult[i] = T[i].gnext;  // prefetched one block ahead (the L1 beside the rings is small)
+                T[i].gnext = (T[i].active && j + 1 < kBlocksPerLane) ? __ldg(T[i].gr + 2 * ((m2 + 1) & 15)) : 0.f;
+                if (KIND == K_FP8 || KIND == K_INT8) mult[i] = T[i].active ? __ldg(T[i].mr + 2 * m2) : 0.f;
+            }
+            uint32_t e[NL][8];
+            const uint32_t* t1[NL];
+#pragma unroll
+            for (int i = 0; i < NL; i++) {
+                e[i][0] = ln[i].sym(tab);
+                t1[i] = tab + kSlots + ((e[i][0] >> 12) & 1u) * kSlots;  // context 1 + c
+            }
+#pragma unroll
+            for (int k = 1; k < 7; k++)
+#pragma unroll
+                for (int i = 0; i < NL; i++) e[i][k] = ln[i].sym(t1[i]);
+#pragma unroll
+            for (int i = 0; i < NL; i++) e[i][7] = ln[i].sym(t1[i] + 2 * kSlots);  // context 3 + c
+            bool esc[NL];
+            bool any = false;
+#pragma unroll
+            for (int i = 0; i < NL; i++) {
+                bool v = ((e[i][0] >> 13) & 0x7Fu) == 0;  // s0 byte 0 or 1
+#pragma unroll
+                for (int k = 1; k < 8; k++) v |= (e[i][k] & 0x000FF000u) == 0;  // byte 0
+                esc[i] = v && T[i].active;
+                any |= esc[i];
+            }
+            const bool slow = __any_sync(0xffffffffu, any);
+#pragma unroll
+            for (int i = 0; i < NL; i++) {
+                float y[8];
+                if (slow) {
+                    const uint32_t c = (e[i][0] >> 12) & 1u;
+                    int32_t B[8];
+#pragma unroll
+                    for (int k = 0; k < 8; k++) B[k] = (int32_t)sym_byte(e[i][k]);
+                    if (esc[i]) {
+#pragma unroll
+                        for (int k = 0; k < 8; k++) {
+                            const bool is_esc = (k == 0) ? (B[0] <= 1) : (B[k] == 0);
+                            if (!is_esc) continue;
+                            const uint32_t hi = ln[i].byte();
+                            const uint32_t lo = ln[i].byte();
+                            const int32_t P = (int32_t)(int16_t)(uint16_t)((hi << 8) | lo);
+                            const int32_t mask = (k == 7) ? 3 : 1;
+                            if (((P - (int32_t)c) & mask) != 0) esc_bad[i] = true;
+                            B[k] = P + 128;
+                        }
+                    }
+                    const int32_t px = B[0] ^ B[1] ^ B[2] ^ B[3] ^ B[4] ^ B[5] ^ B[6];
+                    B[7] += px & 2;
+                    const float cst = -mult[i] * kMagicHiQ;  // exact: mult has <= 7 significant bits
+#pragma unroll
+                    for (int k = 0; k < 8; k++) y[k] = fmaf(__uint_as_float(kMagicHi + (uint32_t)B[k]), mult[i], cst);
+                } else {
+                    uint32_t F[8];
+#pragma unroll
+                    for (int k = 0; k < 8; k++) F[k] = (e[i][k] & 0x000FF000u) | kMagicLo;
+                    // parity of a_0..a_6 is bit 1 of the XOR of the symbol bytes (bit 13 of the entries)
+                    const uint32_t px = e[i][0] ^ e[i][1] ^ e[i][2] ^ e[i][3] ^ e[i][4] ^ e[i][5] ^ e[i][6];
+                    F[7] += px & 0x2000u;
+                    const float cst = -mult[i] * kMagicLoQ;  // exact: mult has <= 7 significant bits
+#pragma unroll
+                    for (int k = 0; k < 8; k++) y[k] = fmaf(__uint_as_float(F[k]), mult[i], cst);
+                }
+                if (T[i].active) {
+                    store_block<KIND>(outp, eoff[i], y);
                     if (DUMP) {
                         uint32_t u[8];
 #pragma unroll
-                        for (int i = 0; i < 8; i++) u[i] = sym_byte(e[i]);
-                        dump_syms(symp, eoff, u);
+                        for (int k = 0; k < 8; k++) u[k] = sym_byte(e[i][k]);
+                        dump_syms(symp, eoff[i], u);
                     }
                 }
-                continue;
+                eoff[i] += step;
             }
-            const float g = gnext;  // prefetched one block ahead (the L1 beside the rings is small)
-            gnext = (active && j + 1 < kBlocksPerLane) ? __ldg(gr + 2 * ((m2 + 1) & 15)) : 0.f;
-            float mult = g;
-            if (KIND == K_FP8 || KIND == K_INT8) mult = active ? __ldg(mr + 2 * m2) : 0.f;
-            uint32_t e[8];
-            e[0] = ln.sym(tab);
-            const uint32_t* t1 = tab + kSlots + ((e[0] >> 12) & 1u) * kSlots;  // context 1 + c
-#pragma unroll
-            for (int i = 1; i < 7; i++) e[i] = ln.sym(t1);
-            e[7] = ln.sym(t1 + 2 * kSlots);  // context 3 + c
-            uint32_t F[8];
-#pragma unroll
-            for (int i = 0; i < 8; i++) F[i] = (e[i] & 0x000FF000u) | kMagicLo;
-            bool esc = F[0] <= kMagicLo + 0x1000u;  // s0 byte 0 or 1
-#pragma unroll
-            for (int i = 1; i < 8; i++) esc |= F[i] == kMagicLo;  // byte 0
-            esc = esc && active;
-            float y[8];
-            if (__any_sync(0xffffffffu, esc)) {
-                const uint32_t c = (e[0] >> 12) & 1u;
-                int32_t B[8];
-#pragma unroll
-                for (int i = 0; i < 8; i++) B[i] = (int32_t)sym_byte(e[i]);
-                if (esc) {
-#pragma unroll
-                    for (int i = 0; i < 8; i++) {
-                        const bool is_esc = (i == 0) ? (B[0] <= 1) : (B[i] == 0);
-                        if (!is_esc) continue;
-                        const uint32_t hi = ln.byte();
-                        const uint32_t lo = ln.byte();
-                        const int32_t P = (int32_t)(int16_t)(uint16_t)((hi << 8) | lo);
-                        const int32_t mask = (i == 7) ? 3 : 1;
-                        if (((P - (int32_t)c) & mask) != 0) esc_bad = true;
-                        B[i] = P + 128;
-                    }
-                }
-                const int32_t px = B[0] ^ B[1] ^ B[2] ^ B[3] ^ B[4] ^ B[5] ^ B[6];
-                B[7] += px & 2;
-                const float cst = -mult * kMagicHiQ;  // exact: mult has <= 7 significant bits
-#pragma unroll
-                for (int i = 0; i < 8; i++) y[i] = fmaf(__uint_as_float(kMagicHi + (uint32_t)B[i]), mult, cst);
-            } else {
-                // parity of a_0..a_6 is bit 1 of the XOR of the symbol bytes (bit 13 of the entries)
-                const uint32_t px = e[0] ^ e[1] ^ e[2] ^ e[3] ^ e[4] ^ e[5] ^ e[6];
-                F[7] += px & 0x2000u;
-                const float cst = -mult * kMagicLoQ;  // exact: mult has <= 7 significant bits
-#pragma unroll
-                for (int i = 0; i < 8; i++) y[i] = fmaf(__uint_as_float(F[i]), mult, cst);
-            }
-            if (active) {
-                store_block<KIND>(outp, eoff, y);
-                if (DUMP) {
-                    uint32_t u[8];
-#pragma unroll
-                    for (int i = 0; i < 8; i++) u[i] = sym_byte(e[i]);
-                    dump_syms(symp, eoff, u);
-                }
-            }
+            }  // lossy
         }
     }
-    if (active && (ln.x != kRansL || ln.a != ln.aend)) flag(status, EP_STATUS_LANE_END);
-    if (esc_bad) flag(status, EP_STATUS_ESCAPE);
+#pragma unroll
+    for (int i = 0; i < NL; i++) {
+        if (T[i].active && (ln[i].x != kRansL || ln[i].a != ln[i].aend)) flag(status, EP_STATUS_LANE_END);
+        if (esc_bad[i]) flag(status, EP_STATUS_ESCAPE);
+    }
 }
 
 __device__ __forceinline__ void copy_row_scales(const DecodeArgs& a, int64_t first, int64_t stride) {
@@ -436,17 +504,26 @@ __host__ __device__ constexpr size_t decode_smem_bytes(int n_ctx) {
     return (size_t)n_ctx * (kSlots + 512) * 4 + kRingBytes;
 }
 
-// byte offset of this thread's ring in g_smem: after the tables and their
-// build scratch of n_ctx contexts (18432 bytes each, a multiple of 128)
+// byte offset of this thread's first ring in g_smem (a thread running NL
+// lanes owns NL consecutive rings): after the tables and their build scratch
+// of n_ctx contexts (18432 bytes each, a multiple of 128)
+template <int NL>
 __device__ __forceinline__ uint32_t lane_ring(int n_ctx) {
-    return (uint32_t)n_ctx * (kSlots + 512) * 4 + 128u * threadIdx.x;
+    return (uint32_t)n_ctx * (kSlots + 512) * 4 + 128u * NL * threadIdx.x;
 }
+
+// Lanes per thread (NL): two interleaved lanes per thread (512 threads) give
+// each warp more independent work and share the per-block overhead, which
+// pays when there are more tile groups than warp slots (the batched kernel,
+// large matrices); a single matrix of less than one wave of groups decodes
+// faster with one lane per thread (1024 threads), since its time is one
+// lane's serial latency.  The symbol-dump debug kernel always uses one.
 
 // ------------------------------------------------------------ single stream
 // Tile groups are dealt round-robin over the CTAs first (group g goes to CTA
 // g % gridDim.x), so a small matrix still spreads over every SM.
-template <int KIND, bool DUMP>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a) {
+template <int KIND, bool DUMP, int NL>
+__global__ void __launch_bounds__(kThreads / NL, 1) decode_kernel(const DecodeArgs a) {
     uint32_t* const smem = g_smem;
     uint32_t* tab = smem;                    // n_ctx x 4096
     uint32_t* fr = smem + a.n_ctx * kSlots;  // n_ctx x 256
@@ -454,10 +531,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     build_tables(a, tab, fr, cu);
     if (KIND == K_FP8 || KIND == K_INT8)
         copy_row_scales(a, (int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
+    // groups are taken NL at a time: warp job p decodes groups NL p .. NL p + NL - 1
     const int64_t n_groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
-    const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta;
-    for (int64_t grp = (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x; grp < n_groups; grp += stride)
-        decode_group<KIND, DUMP>(a, tab, grp, a.status, lane_ring(a.n_ctx));
+    const int64_t n_jobs = (n_groups + NL - 1) / NL;
+    const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t p = (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x; p < n_jobs; p += stride)
+        decode_group<KIND, DUMP, NL>(a, tab, p * NL, a.status, lane_ring<NL>(a.n_ctx));
 }
 
 // ----------------------------------------------------------------- batched
@@ -477,8 +556,12 @@ struct BatchCounters {
 
 constexpr uint32_t kWaitSpins = 1u << 23;  // x ~256 ns sleep: about 2 s before giving up
 
+constexpr int kBatchNL = 2;                              // lanes per thread in the batched kernel
+constexpr int kBatchThreads = kThreads / kBatchNL;      // 512
+constexpr int kGroupsPerUnit = kThreads / 32;           // 32 groups: one per warp and lane slot
+
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBatchThreads, 1)
     batch_kernel(const DecodeArgs* __restrict__ items, const int64_t* __restrict__ unit_start, int64_t n_items,
                  int32_t ring, BatchCounters* ctr, uint32_t* status) {
     uint32_t* const smem = g_smem;
@@ -522,9 +605,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             build_tables(a, tab, smem + a.n_ctx * kSlots, smem + a.n_ctx * kSlots + a.n_ctx * 256);
             cur = item;
         }
-        const int64_t grp = (unit - unit_start[item]) * kWarpsPerCta + (threadIdx.x >> 5);
+        const int64_t grp = (unit - unit_start[item]) * kGroupsPerUnit + (threadIdx.x >> 5) * kBatchNL;
         const int64_t n_groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
-        if (!s_skip && grp < n_groups) decode_group<KIND, false>(a, tab, grp, status, lane_ring(kLossyContexts));
+        if (!s_skip && grp < n_groups)
+            decode_group<KIND, false, kBatchNL>(a, tab, grp, status, lane_ring<kBatchNL>(kLossyContexts));
         if ((KIND == K_FP8 || KIND == K_INT8) && unit == unit_start[item])
             copy_row_scales(a, threadIdx.x, blockDim.x);
         __syncthreads();
@@ -553,20 +637,27 @@ DeviceInfo device_info() {
     return cache[dev];
 }
 
-template <int KIND, bool DUMP>
-ep_status launch(const DecodeArgs& a, size_t smem, cudaStream_t stream) {
+template <int KIND, bool DUMP, int NL>
+ep_status launch_nl(const DecodeArgs& a, size_t smem, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(decode_kernel<KIND, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(decode_kernel<KIND, DUMP, NL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)kMaxSmem);
     });
     if (attr_err != cudaSuccess) return EP_ERR_CUDA;
-    const int64_t groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
+    const int64_t jobs = ((a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp + NL - 1) / NL;
     const int64_t cap = device_info().sms;
-    const int grid = (int)(groups < cap ? groups : cap);
-    decode_kernel<KIND, DUMP><<<grid, kThreads, smem, stream>>>(a);
+    const int grid = (int)(jobs < cap ? jobs : cap);
+    decode_kernel<KIND, DUMP, NL><<<grid, kThreads / NL, smem, stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+template <int KIND, bool DUMP>
+ep_status launch(const DecodeArgs& a, size_t smem, cudaStream_t stream) {
+    const int64_t groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
+    if (DUMP || groups <= (int64_t)device_info().sms * (kThreads / 32)) return launch_nl<KIND, DUMP, 1>(a, smem, stream);
+    return launch_nl<KIND, DUMP, 2>(a, smem, stream);
 }
 
 constexpr size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -628,7 +719,7 @@ ep_status launch_batch(const ep_batch_plan* p, uint32_t* d_status, cudaStream_t 
     const int64_t cap = device_info().sms;
     const int grid = (int)(p->total_units < cap ? p->total_units : cap);
     if (grid <= 0) return EP_OK;
-    batch_kernel<KIND><<<grid, kThreads, smem, stream>>>(
+    batch_kernel<KIND><<<grid, kBatchThreads, smem, stream>>>(
         reinterpret_cast<const DecodeArgs*>(ws + p->items_off), reinterpret_cast<const int64_t*>(ws + p->units_off),
         p->n_items, p->ring, reinterpret_cast<BatchCounters*>(ws + p->counters_off), d_status);
     return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
@@ -701,7 +792,7 @@ ep_status ep_batch_prepare(const ep_batch_item* items, int64_t n_items, int32_t 
         kind = k;
         n_ctx = std::max(n_ctx, L->n_ctx);
         const int64_t groups = (L->n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
-        units[(size_t)i + 1] = units[(size_t)i] + (groups + kWarpsPerCta - 1) / kWarpsPerCta;
+        units[(size_t)i + 1] = units[(size_t)i] + (groups + kGroupsPerUnit - 1) / kGroupsPerUnit;
     }
     delete L;
     if (st != EP_OK) return st;
@@ -830,7 +921,7 @@ extern "C" ep_status ep_batch_decode_static(const ep_batch_item* items, int64_t 
             n_ctx = std::max(n_ctx, L.n_ctx);
             units[i] = unit_total;
             const int64_t groups = (L.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
-            unit_total += (groups + kWarpsPerCta - 1) / kWarpsPerCta;
+            unit_total += (groups + kGroupsPerUnit - 1) / kGroupsPerUnit;
         }
         if (cudaMemcpyAsync(ws + sizeof(DecodeArgs) * (size_t)base, chunk, sizeof(DecodeArgs) * (size_t)n,
                             cudaMemcpyHostToDevice, s) != cudaSuccess ||

@@ -13,8 +13,9 @@
 //   warps 2..5   epilogue: tcgen05.ld of the finished accumulator, BF16
 //                rounding, 16-byte stores of Y, then release of the buffer,
 //                so the epilogue of one tile overlaps the MMAs of the next
-// Output tiles are visited m-fastest, so the CTAs running at the same time
-// share a few W row-slabs and all of X stays resident in the 126 MB L2.
+// Output tiles are visited in groups of 16 token tiles (see tile_coords), so
+// the CTAs running at the same time share a few W row-slabs and the group's
+// rows of X stay resident in the 126 MB L2.
 //
 // ep_compressed_linear decodes the weight stream with the decode kernel of
 // ep_decode.cu into a caller-owned BF16 workspace (78.6 MB for a 10240 x
@@ -49,6 +50,20 @@ struct GemmShape {
     int64_t T, N, K;
     int tiles_m, tiles_n, kblocks;
 };
+
+// Tile order: token tiles in groups of kGroupM; inside a group the CTAs walk
+// the weight slabs n, token tiles fastest.  A wave of 148 tiles then touches
+// kGroupM X row-blocks (16 x 0.98 MB for K = 3840) and a few W slabs, so the
+// group's X stays in L2 while W streams through once per group.
+constexpr int kGroupM = 16;
+
+__device__ __forceinline__ void tile_coords(int t, const GemmShape& sh, int& m, int& n) {
+    const int per_group = kGroupM * sh.tiles_n;
+    const int g = t / per_group, r = t % per_group;
+    const int gm = min(kGroupM, sh.tiles_m - g * kGroupM);  // the last group may be short
+    m = g * kGroupM + r % gm;
+    n = r / gm;
+}
 
 __device__ __forceinline__ void gemm_fail(volatile int* abort_flag, uint32_t* status) {
     *abort_flag = 1;
@@ -98,7 +113,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ------------------------------------------------ TMA producer
         uint32_t s = 0, ph = 0;
         for (int t = blockIdx.x; t < n_tiles && !s_abort; t += gridDim.x) {
-            const int m = t % sh.tiles_m, n = t / sh.tiles_m;
+            int m, n;
+            tile_coords(t, sh, m, n);
             for (int kb = 0; kb < sh.kblocks; kb++) {
                 if (!mbar_wait(&empty[s], ph ^ 1u, globaltimer_ns() + kWaitNs)) {
                     gemm_fail(&s_abort, status);
@@ -153,7 +169,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int q = warp & 3;  // the TMEM lane quarter this warp may read
         uint32_t acc = 0, aph = 0;
         for (int t = blockIdx.x; t < n_tiles && !s_abort; t += gridDim.x) {
-            const int m = t % sh.tiles_m, n = t / sh.tiles_m;
+            int m, n;
+            tile_coords(t, sh, m, n);
             if (!mbar_wait(&tfull[acc], aph, globaltimer_ns() + kWaitNs)) {
                 gemm_fail(&s_abort, status);
                 break;
