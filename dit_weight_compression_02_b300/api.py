@@ -18,8 +18,13 @@ import torch
 
 from ._lib import EpBatchItem, EpBatchPlan, EpInfo, EpParams, EntroPackError, check, lib
 
-CONTAINERS = {"bf16": 0, "fp16": 1, "fp8": 2, "int8": 3}
-CONTAINER_DTYPES = {0: torch.bfloat16, 1: torch.float16, 2: torch.float8_e4m3fn, 3: torch.int8}
+CONTAINERS = {"bf16": 0, "fp16": 1, "fp8": 2, "int8": 3, "fp32": 4}
+CONTAINER_DTYPES = {0: torch.bfloat16, 1: torch.float16, 2: torch.float8_e4m3fn, 3: torch.int8, 4: torch.float32}
+# element types of lossless streams: name -> (container code, numpy bit-pattern type)
+LOSSLESS_DTYPES = {"bf16": (0, np.uint16), "fp16": (1, np.uint16), "fp8": (2, np.uint8), "fp32": (4, np.uint32)}
+_TORCH_TO_LOSSLESS = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float8_e4m3fn: "fp8", torch.float32: "fp32"}
+_BITS_VIEW = {torch.bfloat16: torch.int16, torch.float16: torch.int16, torch.float8_e4m3fn: torch.uint8,
+              torch.float32: torch.int32}
 MODE_LOSSY, MODE_LOSSLESS = 0, 1
 
 
@@ -52,10 +57,33 @@ def bf16_bits(w) -> np.ndarray:
     return a
 
 
+def element_bits(w, dtype: str) -> np.ndarray:
+    """Bit patterns (C-contiguous, host) of a tensor or array holding elements of a lossless dtype."""
+    code, npt = LOSSLESS_DTYPES[dtype]
+    if isinstance(w, torch.Tensor):
+        if _TORCH_TO_LOSSLESS.get(w.dtype) != dtype:
+            raise TypeError(f"tensor dtype {w.dtype} does not match the lossless dtype {dtype}")
+        return w.detach().contiguous().cpu().view(_BITS_VIEW[w.dtype]).numpy().view(npt)
+    a = np.ascontiguousarray(w)
+    if a.dtype != npt:
+        raise TypeError(f"expected {np.dtype(npt).name} bit patterns for {dtype}")
+    return a
+
+
 def encode(w_bits: np.ndarray, target_bpp: float = 4.0, container: str = "bf16", lossless: bool = False,
            sample_frac: float = 0.05, n_threads: int = 0) -> bytes:
-    """ep_encode: BF16 bits (rows x cols) -> stream bytes."""
-    w_bits = bf16_bits(w_bits)
+    """ep_encode: a rows x cols matrix -> stream bytes.
+
+    Lossy: BF16 bits in, decoded into `container`.  Lossless: elements of the
+    type `container` names (bf16, fp16, fp8 or fp32; a torch tensor's own
+    dtype is used when it is one of those), restored bit for bit.
+    """
+    if lossless:
+        if isinstance(w_bits, torch.Tensor) and w_bits.dtype in _TORCH_TO_LOSSLESS:
+            container = _TORCH_TO_LOSSLESS[w_bits.dtype]
+        w_bits = element_bits(w_bits, container)
+    else:
+        w_bits = bf16_bits(w_bits)
     if w_bits.ndim != 2:
         raise ValueError("expected a 2-D weight matrix")
     p = EpParams(MODE_LOSSLESS if lossless else MODE_LOSSY, float(target_bpp), CONTAINERS[container],
@@ -228,7 +256,10 @@ class EntroPackLossyConfig:
 
 @dataclass
 class TileANSConfig:
-    """Lossless tiled ANS of BF16 weights: exponent byte entropy coded, sign+mantissa raw."""
+    """Lossless tiled ANS: the exponent byte (FP8: the whole element) entropy coded, the rest raw.
+
+    Supported element types: BF16, FP16, FP8 e4m3 and FP32 (the tensor's own dtype).
+    """
 
 
 class CompressedTensor:
@@ -251,11 +282,12 @@ class CompressedTensor:
 
 def compress(tensor: torch.Tensor, config=None, device="cuda") -> CompressedTensor:
     config = config or EntroPackLossyConfig()
-    bits = bf16_bits(tensor)
     if isinstance(config, TileANSConfig):
-        blob = encode(bits, lossless=True)
+        if tensor.dtype not in _TORCH_TO_LOSSLESS:
+            raise TypeError(f"lossless compression supports bf16, fp16, float8_e4m3fn and fp32, not {tensor.dtype}")
+        blob = encode(tensor, lossless=True)
     else:
-        blob = encode(bits, config.target_bpp, config.container, sample_frac=config.sample_frac)
+        blob = encode(bf16_bits(tensor), config.target_bpp, config.container, sample_frac=config.sample_frac)
     return CompressedTensor(blob, config, device=device)
 
 

@@ -46,7 +46,16 @@ constexpr float kMagicLoQ = 1600.0f;        // 1536 + 128/2
 constexpr uint32_t kMagicHi = 0x4AC00000u;  // 6291456.0f (spacing 0.5): escape path, any int16 payload
 constexpr float kMagicHiQ = 6291520.0f;     // 6291456 + 128/2
 
-enum Kind { K_BF16 = 0, K_FP16 = 1, K_FP8 = 2, K_INT8 = 3, K_LOSSLESS = 4 };
+// Kernel variants: lossy containers, then lossless streams of 16-bit elements
+// (BF16 / FP16: coded bits 14..7, one raw byte), of FP8 elements (the whole
+// byte coded) and of FP32 elements (coded exponent, three raw bytes).
+enum Kind { K_BF16 = 0, K_FP16 = 1, K_FP8 = 2, K_INT8 = 3, K_LOSSLESS = 4, K_LOSSLESS8 = 5, K_LOSSLESS32 = 6 };
+
+__host__ __device__ constexpr bool is_lossless(int kind) { return kind >= K_LOSSLESS; }
+// raw (uncoded) bytes per element and per tile of a lossless kind
+__host__ __device__ constexpr uint32_t raw_per_elem(int kind) {
+    return kind == K_LOSSLESS ? 1u : (kind == K_LOSSLESS32 ? 3u : 0u);
+}
 
 struct DecodeArgs {
     const uint8_t* blob;
@@ -62,8 +71,8 @@ struct DecodeArgs {
     float* scale_out;
     uint8_t* sym_out;
     uint32_t* status;
-    int64_t rows, cols, n_tiles;
-    int64_t tiles_per_row;
+    int64_t rows, cols, n_tiles;  // true shape (the output is rows x cols, row stride cols)
+    int64_t tiles_per_row;        // tiles per row of the padded grid
 };
 
 // ---------------------------------------------------------------- tables
@@ -287,6 +296,8 @@ struct LaneTile {
     bool active;
     const uint8_t* tb;  // tile payload (lossless: raw bytes first)
     int64_t base;       // output element offset of the lane's block (slab 0, m2 0)
+    int32_t rows_left;  // true rows from the lane's first row on, capped at 32 (blocks with 2 m2 >= rows_left are padding)
+    int64_t col0;       // the lane's first column in slab 0 (blocks at col0 + 16 slab >= cols are padding)
     const float* gr;    // row steps of the lane's rows: gr[2 m2]
     const float* mr;    // FP8/INT8 multipliers: mr[2 m2]
     float gnext;        // row step of the next block (prefetched one block ahead)
@@ -295,7 +306,8 @@ struct LaneTile {
     __device__ __forceinline__ void setup(const DecodeArgs& a, int64_t grp, Lane& ln, uint32_t ring_off,
                                           uint32_t* status) {
         const int lane = threadIdx.x & 31, l = lane & 3, tig = lane >> 2;
-        constexpr uint32_t kHdr = (KIND == K_LOSSLESS ? kRawBytesPerTile : 0) + kTileHeaderBytes;
+        constexpr uint32_t kRaw = 4096u * raw_per_elem(KIND);
+        constexpr uint32_t kHdr = kRaw + kTileHeaderBytes;
         const int64_t tile = grp * kTilesPerWarp + tig;
         active = grp >= 0 && tile < a.n_tiles;
         uint64_t o0 = 0, o1 = 0;
@@ -308,7 +320,7 @@ struct LaneTile {
             }
         }
         tb = a.payload + (active ? o0 : 0);
-        const uint8_t* th = tb + (KIND == K_LOSSLESS ? kRawBytesPerTile : 0);
+        const uint8_t* th = tb + kRaw;
         ln.x = kRansL;
         ln.pay = a.payload;
         ln.roff = ring_off;
@@ -336,14 +348,18 @@ struct LaneTile {
         // this lane's block of step j sits at tile row 2 (j % 16) + l / 2 and
         // tile column 16 (j / 16) + 8 (l % 2)
         const int64_t row0 = tr0 + (l >> 1);
-        base = row0 * a.cols + tc0 + 8 * (l & 1);
+        rows_left = (int32_t)min(a.rows - row0, (int64_t)kTileRows);
+        col0 = tc0 + 8 * (l & 1);
+        base = row0 * a.cols + col0;
         gr = a.g + row0;
         mr = a.m + row0;
         gnext = active ? __ldg(gr) : 0.f;
     }
 };
 
-template <int KIND, bool DUMP, int NL>
+// RAGGED: the stream's shape is not a whole number of tiles, so blocks in the
+// padding must not be stored (the tile-aligned variant skips those checks).
+template <int KIND, bool DUMP, int NL, bool RAGGED>
 __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t* tab, int64_t grp0,
                                              uint32_t* status, uint32_t ring_off) {
     // fields used inside the block loop, read once: the batched kernel's
@@ -363,13 +379,17 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
 
     for (int slab = 0; slab < 8; slab++) {
         int64_t eoff[NL];
+        bool col_in[NL];  // the slab's block lies inside the true columns
 #pragma unroll
-        for (int i = 0; i < NL; i++) eoff[i] = T[i].base + 16 * slab;
+        for (int i = 0; i < NL; i++) {
+            eoff[i] = T[i].base + 16 * slab;
+            col_in[i] = T[i].active && (!RAGGED || T[i].col0 + 16 * slab < a.cols);
+        }
 #pragma unroll 2
         for (int m2 = 0; m2 < 16; m2++) {
             const int j = slab * 16 + m2;
             top_up<NL>(ln);
-            if constexpr (KIND == K_LOSSLESS) {
+            if constexpr (is_lossless(KIND)) {
                 uint32_t e[NL][8];
 #pragma unroll
                 for (int k = 0; k < 8; k++)
@@ -377,20 +397,56 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
                     for (int i = 0; i < NL; i++) e[i][k] = ln[i].sym(tab);
 #pragma unroll
                 for (int i = 0; i < NL; i++) {
-                    uint2 raw = make_uint2(0, 0);
-                    if (T[i].active) raw = *reinterpret_cast<const uint2*>(T[i].tb + 8 * (4 * j + l));
-                    uint32_t w[4];
+                    const bool st = col_in[i] && (!RAGGED || 2 * m2 < T[i].rows_left);
+                    // raw bytes of block 4 j + l start at raw_per_elem * 8 * (4 j + l)
+                    const uint8_t* rp = T[i].tb + raw_per_elem(KIND) * 8 * (4 * j + l);
+                    if constexpr (KIND == K_LOSSLESS) {
+                        uint2 raw = make_uint2(0, 0);
+                        if (T[i].active) raw = *reinterpret_cast<const uint2*>(rp);
+                        uint32_t w[4];
 #pragma unroll
-                    for (int h = 0; h < 4; h++) {
-                        const uint32_t rw = (h < 2 ? raw.x : raw.y) >> (16 * (h & 1));
-                        const uint32_t r0 = rw & 0xFFu, r1 = (rw >> 8) & 0xFFu;
-                        const uint32_t v0 = ((r0 & 0x80u) << 8) | ((e[i][2 * h] >> 5) & 0x7F80u) | (r0 & 0x7Fu);
-                        const uint32_t v1 = ((r1 & 0x80u) << 8) | ((e[i][2 * h + 1] >> 5) & 0x7F80u) | (r1 & 0x7Fu);
-                        w[h] = v0 | (v1 << 16);
+                        for (int h = 0; h < 4; h++) {
+                            const uint32_t rw = (h < 2 ? raw.x : raw.y) >> (16 * (h & 1));
+                            const uint32_t r0 = rw & 0xFFu, r1 = (rw >> 8) & 0xFFu;
+                            const uint32_t v0 = ((r0 & 0x80u) << 8) | ((e[i][2 * h] >> 5) & 0x7F80u) | (r0 & 0x7Fu);
+                            const uint32_t v1 =
+                                ((r1 & 0x80u) << 8) | ((e[i][2 * h + 1] >> 5) & 0x7F80u) | (r1 & 0x7Fu);
+                            w[h] = v0 | (v1 << 16);
+                        }
+                        if (st)
+                            *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(outp) + eoff[i]) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
+                    } else if constexpr (KIND == K_LOSSLESS8) {
+                        uint32_t u[8];
+#pragma unroll
+                        for (int k = 0; k < 8; k++) u[k] = sym_byte(e[i][k]);
+                        if (st)
+                            *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(outp) + eoff[i]) =
+                                make_uint2(u[0] | (u[1] << 8) | (u[2] << 16) | (u[3] << 24),
+                                           u[4] | (u[5] << 8) | (u[6] << 16) | (u[7] << 24));
+                    } else {  // K_LOSSLESS32: 24 raw bytes per block, 3 per element
+                        uint32_t r[6] = {0, 0, 0, 0, 0, 0};
+                        if (T[i].active) {
+                            const uint2* rq = reinterpret_cast<const uint2*>(rp);  // 24 * block: 8-byte aligned
+                            const uint2 q0 = rq[0], q1 = rq[1], q2 = rq[2];
+                            r[0] = q0.x; r[1] = q0.y; r[2] = q1.x; r[3] = q1.y; r[4] = q2.x; r[5] = q2.y;
+                        }
+                        uint32_t v[8];
+#pragma unroll
+                        for (int k = 0; k < 8; k++) {
+                            // raw bytes 3k .. 3k + 2 of the block (little-endian in r[])
+                            const uint32_t b0 = (r[(3 * k) >> 2] >> (8 * ((3 * k) & 3))) & 0xFFu;
+                            const uint32_t b1 = (r[(3 * k + 1) >> 2] >> (8 * ((3 * k + 1) & 3))) & 0xFFu;
+                            const uint32_t b2 = (r[(3 * k + 2) >> 2] >> (8 * ((3 * k + 2) & 3))) & 0xFFu;
+                            v[k] = ((b0 & 0x80u) << 24) | (sym_byte(e[i][k]) << 23) | ((b0 & 0x7Fu) << 16) | (b1 << 8) | b2;
+                        }
+                        if (st) {
+                            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(outp) + eoff[i]);
+                            dst[0] = make_uint4(v[0], v[1], v[2], v[3]);
+                            dst[1] = make_uint4(v[4], v[5], v[6], v[7]);
+                        }
                     }
-                    if (T[i].active) {
-                        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(outp) + eoff[i]) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
+                    if (st) {
                         if (DUMP) {
                             uint32_t u[8];
 #pragma unroll
@@ -469,7 +525,7 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
 #pragma unroll
                     for (int k = 0; k < 8; k++) y[k] = fmaf(__uint_as_float(F[k]), mult[i], cst);
                 }
-                if (T[i].active) {
+                if (col_in[i] && (!RAGGED || 2 * m2 < T[i].rows_left)) {
                     store_block<KIND>(outp, eoff[i], y);
                     if (DUMP) {
                         uint32_t u[8];
@@ -522,7 +578,7 @@ __device__ __forceinline__ uint32_t lane_ring(int n_ctx) {
 // ------------------------------------------------------------ single stream
 // Tile groups are dealt round-robin over the CTAs first (group g goes to CTA
 // g % gridDim.x), so a small matrix still spreads over every SM.
-template <int KIND, bool DUMP, int NL>
+template <int KIND, bool DUMP, int NL, bool RAGGED>
 __global__ void __launch_bounds__(kThreads / NL, 1) decode_kernel(const DecodeArgs a) {
     uint32_t* const smem = g_smem;
     uint32_t* tab = smem;                    // n_ctx x 4096
@@ -536,7 +592,7 @@ __global__ void __launch_bounds__(kThreads / NL, 1) decode_kernel(const DecodeAr
     const int64_t n_jobs = (n_groups + NL - 1) / NL;
     const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 5);
     for (int64_t p = (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x; p < n_jobs; p += stride)
-        decode_group<KIND, DUMP, NL>(a, tab, p * NL, a.status, lane_ring<NL>(a.n_ctx));
+        decode_group<KIND, DUMP, NL, RAGGED>(a, tab, p * NL, a.status, lane_ring<NL>(a.n_ctx));
 }
 
 // ----------------------------------------------------------------- batched
@@ -560,7 +616,7 @@ constexpr int kBatchNL = 2;                              // lanes per thread in 
 constexpr int kBatchThreads = kThreads / kBatchNL;      // 512
 constexpr int kGroupsPerUnit = kThreads / 32;           // 32 groups: one per warp and lane slot
 
-template <int KIND>
+template <int KIND, bool RAGGED>
 __global__ void __launch_bounds__(kBatchThreads, 1)
     batch_kernel(const DecodeArgs* __restrict__ items, const int64_t* __restrict__ unit_start, int64_t n_items,
                  int32_t ring, BatchCounters* ctr, uint32_t* status) {
@@ -608,7 +664,7 @@ __global__ void __launch_bounds__(kBatchThreads, 1)
         const int64_t grp = (unit - unit_start[item]) * kGroupsPerUnit + (threadIdx.x >> 5) * kBatchNL;
         const int64_t n_groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
         if (!s_skip && grp < n_groups)
-            decode_group<KIND, false, kBatchNL>(a, tab, grp, status, lane_ring<kBatchNL>(kLossyContexts));
+            decode_group<KIND, false, kBatchNL, RAGGED>(a, tab, grp, status, lane_ring<kBatchNL>(kLossyContexts));
         if ((KIND == K_FP8 || KIND == K_INT8) && unit == unit_start[item])
             copy_row_scales(a, threadIdx.x, blockDim.x);
         __syncthreads();
@@ -637,27 +693,36 @@ DeviceInfo device_info() {
     return cache[dev];
 }
 
-template <int KIND, bool DUMP, int NL>
+template <int KIND, bool DUMP, int NL, bool RAGGED>
 ep_status launch_nl(const DecodeArgs& a, size_t smem, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(decode_kernel<KIND, DUMP, NL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kMaxSmem);
+        attr_err = cudaFuncSetAttribute(decode_kernel<KIND, DUMP, NL, RAGGED>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
     });
     if (attr_err != cudaSuccess) return EP_ERR_CUDA;
     const int64_t jobs = ((a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp + NL - 1) / NL;
     const int64_t cap = device_info().sms;
     const int grid = (int)(jobs < cap ? jobs : cap);
-    decode_kernel<KIND, DUMP, NL><<<grid, kThreads / NL, smem, stream>>>(a);
+    decode_kernel<KIND, DUMP, NL, RAGGED><<<grid, kThreads / NL, smem, stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+bool is_ragged(int64_t rows, int64_t cols) { return (rows % kTileRows) != 0 || (cols % kTileCols) != 0; }
+
+template <int KIND, bool DUMP, bool RAGGED>
+ep_status launch_r(const DecodeArgs& a, size_t smem, cudaStream_t stream) {
+    const int64_t groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
+    if (DUMP || groups <= (int64_t)device_info().sms * (kThreads / 32))
+        return launch_nl<KIND, DUMP, 1, RAGGED>(a, smem, stream);
+    return launch_nl<KIND, DUMP, 2, RAGGED>(a, smem, stream);
 }
 
 template <int KIND, bool DUMP>
 ep_status launch(const DecodeArgs& a, size_t smem, cudaStream_t stream) {
-    const int64_t groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
-    if (DUMP || groups <= (int64_t)device_info().sms * (kThreads / 32)) return launch_nl<KIND, DUMP, 1>(a, smem, stream);
-    return launch_nl<KIND, DUMP, 2>(a, smem, stream);
+    return is_ragged(a.rows, a.cols) ? launch_r<KIND, DUMP, true>(a, smem, stream)
+                                     : launch_r<KIND, DUMP, false>(a, smem, stream);
 }
 
 constexpr size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -688,8 +753,8 @@ ep_status fill_args(const uint8_t* h_blob, const void* d_blob, size_t bytes, voi
     a->payload = db + L.payload_off;
     a->payload_bytes = L.total - L.payload_off;
     a->g = reinterpret_cast<const float*>(db + L.rowmeta_off);
-    a->m = a->g + L.rows;
-    a->t = a->g + 2 * L.rows;
+    a->m = a->g + L.rows_p;  // row metadata covers the padded rows
+    a->t = a->g + 2 * L.rows_p;
     for (int c = 0; c < L.n_ctx; c++) a->ctx_off[c] = (uint32_t)L.ctx_off[c];
     a->n_ctx = L.n_ctx;
     a->out = d_out;
@@ -699,18 +764,21 @@ ep_status fill_args(const uint8_t* h_blob, const void* d_blob, size_t bytes, voi
     a->rows = L.rows;
     a->cols = L.cols;
     a->n_tiles = L.n_tiles;
-    a->tiles_per_row = L.cols / kTileCols;
+    a->tiles_per_row = L.cols_p / kTileCols;
     return EP_OK;
 }
 
-int kind_of(const Layout& L) { return L.mode == EP_MODE_LOSSLESS_TILEANS ? K_LOSSLESS : L.container; }
+int kind_of(const Layout& L) {
+    if (L.mode != EP_MODE_LOSSLESS_TILEANS) return L.container;
+    return L.container == EP_C_FP8_E4M3 ? K_LOSSLESS8 : (L.container == EP_C_FP32 ? K_LOSSLESS32 : K_LOSSLESS);
+}
 
-template <int KIND>
-ep_status launch_batch(const ep_batch_plan* p, uint32_t* d_status, cudaStream_t stream) {
+template <int KIND, bool RAGGED>
+ep_status launch_batch_r(const ep_batch_plan* p, uint32_t* d_status, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(batch_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(batch_kernel<KIND, RAGGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)kMaxSmem);
     });
     if (attr_err != cudaSuccess) return EP_ERR_CUDA;
@@ -719,10 +787,16 @@ ep_status launch_batch(const ep_batch_plan* p, uint32_t* d_status, cudaStream_t 
     const int64_t cap = device_info().sms;
     const int grid = (int)(p->total_units < cap ? p->total_units : cap);
     if (grid <= 0) return EP_OK;
-    batch_kernel<KIND><<<grid, kBatchThreads, smem, stream>>>(
+    batch_kernel<KIND, RAGGED><<<grid, kBatchThreads, smem, stream>>>(
         reinterpret_cast<const DecodeArgs*>(ws + p->items_off), reinterpret_cast<const int64_t*>(ws + p->units_off),
         p->n_items, p->ring, reinterpret_cast<BatchCounters*>(ws + p->counters_off), d_status);
     return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+// plan->reserved != 0: some item's shape is not a whole number of tiles
+template <int KIND>
+ep_status launch_batch(const ep_batch_plan* p, uint32_t* d_status, cudaStream_t stream) {
+    return p->reserved ? launch_batch_r<KIND, true>(p, d_status, stream) : launch_batch_r<KIND, false>(p, d_status, stream);
 }
 
 ep_status decode_impl(const uint8_t* h_blob, const void* d_blob, size_t bytes, void* d_out, float* d_scale,
@@ -740,6 +814,10 @@ ep_status decode_impl(const uint8_t* h_blob, const void* d_blob, size_t bytes, v
         case K_FP16: return dump ? launch<K_FP16, true>(a, smem, stream) : launch<K_FP16, false>(a, smem, stream);
         case K_FP8: return dump ? launch<K_FP8, true>(a, smem, stream) : launch<K_FP8, false>(a, smem, stream);
         case K_INT8: return dump ? launch<K_INT8, true>(a, smem, stream) : launch<K_INT8, false>(a, smem, stream);
+        case K_LOSSLESS8:
+            return dump ? launch<K_LOSSLESS8, true>(a, smem, stream) : launch<K_LOSSLESS8, false>(a, smem, stream);
+        case K_LOSSLESS32:
+            return dump ? launch<K_LOSSLESS32, true>(a, smem, stream) : launch<K_LOSSLESS32, false>(a, smem, stream);
         default: return dump ? launch<K_LOSSLESS, true>(a, smem, stream) : launch<K_LOSSLESS, false>(a, smem, stream);
     }
 }
@@ -780,6 +858,7 @@ ep_status ep_batch_prepare(const ep_batch_item* items, int64_t n_items, int32_t 
     Layout* L = new (std::nothrow) Layout();
     if (!L) return EP_ERR_NOMEM;
     int kind = -1, n_ctx = 0;
+    bool ragged = false;
     ep_status st = EP_OK;
     for (int64_t i = 0; i < n_items && st == EP_OK; i++) {
         const ep_batch_item& it = items[i];
@@ -791,6 +870,7 @@ ep_status ep_batch_prepare(const ep_batch_item* items, int64_t n_items, int32_t 
         if (kind >= 0 && k != kind) st = EP_ERR_INVALID_ARG;  // one container/mode per batch
         kind = k;
         n_ctx = std::max(n_ctx, L->n_ctx);
+        ragged = ragged || is_ragged(L->rows, L->cols);
         const int64_t groups = (L->n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
         units[(size_t)i + 1] = units[(size_t)i] + (groups + kGroupsPerUnit - 1) / kGroupsPerUnit;
     }
@@ -808,6 +888,7 @@ ep_status ep_batch_prepare(const ep_batch_item* items, int64_t n_items, int32_t 
     plan->ring = ring;
     plan->kind = kind;
     plan->n_ctx = n_ctx;
+    plan->reserved = ragged ? 1 : 0;
     plan->d_workspace = d_workspace;
     plan->workspace_bytes = workspace_bytes;
     plan->items_off = items_off;
@@ -830,6 +911,8 @@ ep_status ep_batch_decode(const ep_batch_plan* plan, uint32_t* d_status, ep_stre
         case K_FP8: return launch_batch<K_FP8>(plan, d_status, s);
         case K_INT8: return launch_batch<K_INT8>(plan, d_status, s);
         case K_LOSSLESS: return launch_batch<K_LOSSLESS>(plan, d_status, s);
+        case K_LOSSLESS8: return launch_batch<K_LOSSLESS8>(plan, d_status, s);
+        case K_LOSSLESS32: return launch_batch<K_LOSSLESS32>(plan, d_status, s);
     }
     return EP_ERR_INVALID_ARG;
 }
@@ -908,6 +991,7 @@ extern "C" ep_status ep_batch_decode_static(const ep_batch_item* items, int64_t 
     int64_t units[kChunk + 1];
     int64_t unit_total = 0;
     int kind = -1, n_ctx = 0;
+    bool ragged = false;
     for (int64_t base = 0; base < n_items; base += kChunk) {
         const int64_t n = std::min<int64_t>(kChunk, n_items - base);
         for (int64_t i = 0; i < n; i++) {
@@ -919,6 +1003,7 @@ extern "C" ep_status ep_batch_decode_static(const ep_batch_item* items, int64_t 
             if (kind >= 0 && k != kind) return EP_ERR_INVALID_ARG;  // one container/mode per batch
             kind = k;
             n_ctx = std::max(n_ctx, L.n_ctx);
+            ragged = ragged || is_ragged(L.rows, L.cols);
             units[i] = unit_total;
             const int64_t groups = (L.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
             unit_total += (groups + kGroupsPerUnit - 1) / kGroupsPerUnit;
@@ -945,6 +1030,7 @@ extern "C" ep_status ep_batch_decode_static(const ep_batch_item* items, int64_t 
     plan.ring = ring;
     plan.kind = kind;
     plan.n_ctx = n_ctx;
+    plan.reserved = ragged ? 1 : 0;
     plan.d_workspace = ws;
     plan.workspace_bytes = kStaticScratchBytes;
     plan.items_off = 0;
@@ -956,6 +1042,8 @@ extern "C" ep_status ep_batch_decode_static(const ep_batch_item* items, int64_t 
         case K_FP8: return launch_batch<K_FP8>(&plan, d_status, s);
         case K_INT8: return launch_batch<K_INT8>(&plan, d_status, s);
         case K_LOSSLESS: return launch_batch<K_LOSSLESS>(&plan, d_status, s);
+        case K_LOSSLESS8: return launch_batch<K_LOSSLESS8>(&plan, d_status, s);
+        case K_LOSSLESS32: return launch_batch<K_LOSSLESS32>(&plan, d_status, s);
     }
     return EP_ERR_INVALID_ARG;
 }

@@ -301,14 +301,15 @@ ep_status write_blob(const Writer& W, std::vector<TileBytes>& tiles, int threads
 }
 
 // tile payload from (raw?, lane states, lane words)
-void pack_tile(const uint8_t* raw, const uint32_t* st, std::vector<uint16_t>* words, TileBytes& out) {
-    uint64_t n = (raw ? kRawBytesPerTile : 0) + kTileHeaderBytes;
+void pack_tile(const uint8_t* raw, size_t raw_len, const uint32_t* st, std::vector<uint16_t>* words,
+               TileBytes& out) {
+    uint64_t n = (raw ? raw_len : 0) + kTileHeaderBytes;
     for (int l = 0; l < kLanes; l++) n += 2 * words[l].size();
     out.bytes.assign(up16(n), 0);
     uint8_t* p = out.bytes.data();
     if (raw) {
-        std::memcpy(p, raw, kRawBytesPerTile);
-        p += kRawBytesPerTile;
+        std::memcpy(p, raw, raw_len);
+        p += raw_len;
     }
     for (int l = 0; l < kLanes; l++, p += 4) std::memcpy(p, &st[l], 4);
     for (int l = 0; l < kLanes; l++, p += 2) {
@@ -324,8 +325,11 @@ void pack_tile(const uint8_t* raw, const uint32_t* st, std::vector<uint16_t>* wo
 // ------------------------------------------------------------ lossy encode
 class LossyEncoder {
    public:
-    LossyEncoder(const uint16_t* w, int64_t M, int64_t K, const ep_params& p, int threads)
-        : w_(w), M_(M), K_(K), p_(p), threads_(threads) {}
+    // w: the matrix padded with zeros to whole tiles (M x K, both multiples of
+    // the tile); Mt x Kt: the true shape, which alone enters the row statistics,
+    // the rate estimate and the header
+    LossyEncoder(const uint16_t* w, int64_t M, int64_t K, int64_t Mt, int64_t Kt, const ep_params& p, int threads)
+        : w_(w), M_(M), K_(K), Mt_(Mt), Kt_(Kt), p_(p), threads_(threads) {}
 
     ep_status run(uint8_t** blob, size_t* bytes) {
         row_stats();
@@ -351,14 +355,15 @@ class LossyEncoder {
             meta.insert(meta.end(), mult_.begin(), mult_.end());
             meta.insert(meta.end(), tscale_.begin(), tscale_.end());
         }
-        Writer W{0, p_.container, kLossyContexts, M_, K_, (int64_t)tiles.size(), p_.target_bpp, j,
+        Writer W{0, p_.container, kLossyContexts, Mt_, Kt_, (int64_t)tiles.size(), p_.target_bpp, j,
                  (uint32_t)sample_rows(), T_.f, meta.data(), (uint64_t)meta.size()};
         return write_blob(W, tiles, threads_, blob, bytes);
     }
 
    private:
     const uint16_t* w_;
-    int64_t M_, K_;
+    int64_t M_, K_;    // padded shape (row stride K_)
+    int64_t Mt_, Kt_;  // true shape
     ep_params p_;
     int threads_;
     RowInfo rows_;
@@ -367,19 +372,20 @@ class LossyEncoder {
     uint64_t counts_[kLossyContexts][256] = {{0}};
     SymTable T_{};
 
+    // RMS and peak of each true row over its true columns; padding rows stay 0
     void row_stats() {
         rows_.rms.assign((size_t)M_, 0.0);
         rows_.peak.assign((size_t)M_, 0.0);
-        parallel_for(M_, threads_, [&](int64_t r0, int64_t r1, int) {
+        parallel_for(Mt_, threads_, [&](int64_t r0, int64_t r1, int) {
             for (int64_t r = r0; r < r1; r++) {
                 const uint16_t* row = w_ + r * K_;
                 double s = 0.0, pk = 0.0;
-                for (int64_t k = 0; k < K_; k++) {
+                for (int64_t k = 0; k < Kt_; k++) {
                     double v = bf16_value(row[k]);
                     s += v * v;
                     pk = std::max(pk, std::fabs(v));
                 }
-                rows_.rms[r] = std::sqrt(s / (double)K_);
+                rows_.rms[r] = std::sqrt(s / (double)Kt_);
                 rows_.peak[r] = pk;
             }
         });
@@ -395,9 +401,9 @@ class LossyEncoder {
     }
 
     int64_t sample_rows() const {
-        const double want = std::ceil((double)p_.sample_frac * (double)M_);
+        const double want = std::ceil((double)p_.sample_frac * (double)Mt_);
         int64_t n = want >= 1.0 ? (int64_t)want : 1;
-        return std::min<int64_t>(std::max<int64_t>(n, 1), M_);
+        return std::min<int64_t>(std::max<int64_t>(n, 1), Mt_);
     }
 
     // bits per parameter of the coded symbols on the row sample at index j
@@ -408,9 +414,9 @@ class LossyEncoder {
         parallel_for(ns, T, [&](int64_t i0, int64_t i1, int t) {
             uint64_t* H = hist.data() + (size_t)t * kLossyContexts * 256;
             for (int64_t i = i0; i < i1; i++) {
-                const int64_t r = (int64_t)(((unsigned __int128)i * (uint64_t)M_) / (uint64_t)ns);
+                const int64_t r = (int64_t)(((unsigned __int128)i * (uint64_t)Mt_) / (uint64_t)ns);
                 const double g = (double)(float)step_of(rows_.rms[r], j);
-                for (int64_t k0 = 0; k0 < K_; k0 += 8) {
+                for (int64_t k0 = 0; k0 < Kt_; k0 += 8) {
                     BlockCode bc;
                     block(r, k0, g, &bc);
                     esc[t] += bc.n_esc;
@@ -430,7 +436,7 @@ class LossyEncoder {
             for (int u = 0; u < 256; u++)
                 if (cnt[u]) bits += (double)cnt[u] * std::log2((double)N / (double)cnt[u]);
         }
-        return (bits + 16.0 * (double)n_esc) / (double)(ns * K_);
+        return (bits + 16.0 * (double)n_esc) / (double)(ns * Kt_);
     }
 
     int choose_j() const {
@@ -558,7 +564,7 @@ class LossyEncoder {
                         words[l].size() > 65535)
                         bad = true;
                 }
-                pack_tile(nullptr, st, words, tiles[(size_t)t]);
+                pack_tile(nullptr, 0, st, words, tiles[(size_t)t]);
             }
         });
         return bad ? EP_ERR_UNSUPPORTED : EP_OK;
@@ -566,11 +572,36 @@ class LossyEncoder {
 };
 
 // --------------------------------------------------------- lossless encode
-ep_status encode_lossless(const uint16_t* w, int64_t M, int64_t K, int threads, uint8_t** blob, size_t* bytes) {
+// Element split (FORMAT.md §5): the coded byte and the raw bytes of one element.
+struct LosslessSplit {
+    int container, eb, rb;  // element type, element bytes, raw bytes per element
+    uint8_t code(const uint8_t* x, uint8_t* raw) const {
+        if (container == EP_C_FP8_E4M3) return x[0];
+        if (container == EP_C_FP32) {
+            uint32_t v;
+            std::memcpy(&v, x, 4);
+            raw[0] = (uint8_t)(((v >> 24) & 0x80u) | ((v >> 16) & 0x7Fu));
+            raw[1] = (uint8_t)(v >> 8);
+            raw[2] = (uint8_t)v;
+            return (uint8_t)(v >> 23);
+        }
+        uint16_t v;
+        std::memcpy(&v, x, 2);
+        raw[0] = (uint8_t)(((v >> 8) & 0x80u) | (v & 0x7Fu));
+        return (uint8_t)(v >> 7);
+    }
+};
+
+// w: the matrix padded to whole tiles (M x K elements of `container`);
+// Mt x Kt: the true shape (header only)
+ep_status encode_lossless(const uint8_t* w, int64_t M, int64_t K, int64_t Mt, int64_t Kt, int container,
+                         int threads, uint8_t** blob, size_t* bytes) {
+    const LosslessSplit sp{container, (int)container_bytes(container), lossless_raw_per_elem(container)};
     std::vector<uint64_t> hist((size_t)threads * 256, 0);
     parallel_for(M, threads, [&](int64_t r0, int64_t r1, int t) {
         uint64_t* H = hist.data() + (size_t)t * 256;
-        for (int64_t i = r0 * K; i < r1 * K; i++) H[(w[i] >> 7) & 0xFF]++;
+        uint8_t scratch[3];
+        for (int64_t i = r0 * K; i < r1 * K; i++) H[sp.code(w + (size_t)i * sp.eb, scratch)]++;
     });
     uint64_t cnt[256] = {0};
     for (int t = 0; t < threads; t++)
@@ -583,17 +614,19 @@ ep_status encode_lossless(const uint16_t* w, int64_t M, int64_t K, int threads, 
         acc += T.f[0][u];
     }
     const int64_t tpr = K / kTileCols, n_tiles = (M / kTileRows) * tpr;
+    const size_t raw_len = (size_t)sp.rb * 4096;
     std::vector<TileBytes> tiles((size_t)n_tiles);
     parallel_for(n_tiles, threads, [&](int64_t t0, int64_t t1, int) {
-        uint8_t raw[kRawBytesPerTile], sym[kBlocksPerLane * 8], ctx[kBlocksPerLane * 8] = {0};
+        std::vector<uint8_t> raw(raw_len ? raw_len : 1);
+        uint8_t sym[kBlocksPerLane * 8], ctx[kBlocksPerLane * 8] = {0}, scratch[3];
         std::vector<uint16_t> words[kLanes];
         for (int64_t t = t0; t < t1; t++) {
             const int64_t r0 = (t / tpr) * kTileRows, c0 = (t % tpr) * kTileCols;
             for (int b = 0; b < kBlocksPerTile; b++) {
                 int br, bc;
                 tile_block(b, &br, &bc);
-                const uint16_t* src = w + (r0 + br) * K + c0 + bc;
-                for (int q = 0; q < 8; q++) raw[8 * b + q] = (uint8_t)(((src[q] >> 8) & 0x80) | (src[q] & 0x7F));
+                const uint8_t* src = w + (size_t)((r0 + br) * K + c0 + bc) * sp.eb;
+                for (int q = 0; q < 8; q++) sp.code(src + (size_t)q * sp.eb, raw.data() + (size_t)sp.rb * (8 * b + q));
             }
             uint32_t st[kLanes];
             for (int l = 0; l < kLanes; l++) {
@@ -601,35 +634,50 @@ ep_status encode_lossless(const uint16_t* w, int64_t M, int64_t K, int threads, 
                 for (int b = l; b < kBlocksPerTile; b += kLanes) {
                     int br, bc;
                     tile_block(b, &br, &bc);
-                    const uint16_t* src = w + (r0 + br) * K + c0 + bc;
-                    for (int q = 0; q < 8; q++) sym[n++] = (uint8_t)((src[q] >> 7) & 0xFF);
+                    const uint8_t* src = w + (size_t)((r0 + br) * K + c0 + bc) * sp.eb;
+                    for (int q = 0; q < 8; q++) sym[n++] = sp.code(src + (size_t)q * sp.eb, scratch);
                 }
                 rans_lane(sym, ctx, n, T, &st[l], words[l]);
             }
-            pack_tile(raw, st, words, tiles[(size_t)t]);
+            pack_tile(sp.rb ? raw.data() : nullptr, raw_len, st, words, tiles[(size_t)t]);
         }
     });
-    Writer W{1, EP_C_BF16, 1, M, K, n_tiles, 0.f, 0, 0u, T.f, nullptr, 0};
+    Writer W{1, container, 1, Mt, Kt, n_tiles, 0.f, 0, 0u, T.f, nullptr, 0};
     return write_blob(W, tiles, threads, blob, bytes);
 }
 
 }  // namespace
 }  // namespace ep
 
-extern "C" ep_status ep_encode(const uint16_t* w, int64_t rows, int64_t cols, const ep_params* p, uint8_t** blob,
+extern "C" ep_status ep_encode(const void* w_in, int64_t rows, int64_t cols, const ep_params* p, uint8_t** blob,
                                size_t* blob_bytes) {
+    const uint16_t* w = static_cast<const uint16_t*>(w_in);  // lossy input: BF16 bit patterns
     if (!w || !p || !blob || !blob_bytes) return EP_ERR_INVALID_ARG;
     *blob = nullptr;
     *blob_bytes = 0;
-    if (rows <= 0 || cols <= 0 || rows % ep::kTileRows || cols % ep::kTileCols) return EP_ERR_SHAPE;
+    if (rows <= 0 || cols <= 0 || cols % 8) return EP_ERR_SHAPE;
+    if (rows > ((int64_t)1 << 40) || cols > ((int64_t)1 << 40)) return EP_ERR_SHAPE;
     if (p->mode != EP_MODE_LOSSY_E8 && p->mode != EP_MODE_LOSSLESS_TILEANS) return EP_ERR_INVALID_ARG;
     int threads = p->n_threads > 0 ? p->n_threads : (int)std::max(1u, std::thread::hardware_concurrency());
     threads = std::min(threads, 256);
     try {
-        if (p->mode == EP_MODE_LOSSLESS_TILEANS) {
-            if (p->container != EP_C_BF16) return EP_ERR_INVALID_ARG;
-            return ep::encode_lossless(w, rows, cols, threads, blob, blob_bytes);
+        // tiles cover the matrix padded with zeros to whole 32 x 128 tiles
+        const int64_t Mp = (rows + ep::kTileRows - 1) / ep::kTileRows * ep::kTileRows;
+        const int64_t Kp = (cols + ep::kTileCols - 1) / ep::kTileCols * ep::kTileCols;
+        const bool lossless = p->mode == EP_MODE_LOSSLESS_TILEANS;
+        if (lossless && !ep::lossless_container_ok(p->container)) return EP_ERR_INVALID_ARG;
+        const size_t eb = lossless ? ep::container_bytes(p->container) : sizeof(uint16_t);
+        std::vector<uint8_t> padded;
+        const uint8_t* wp = static_cast<const uint8_t*>(w_in);
+        if (Mp != rows || Kp != cols) {
+            padded.assign((size_t)(Mp * Kp) * eb, 0);
+            ep::parallel_for(rows, threads, [&](int64_t r0, int64_t r1, int) {
+                for (int64_t r = r0; r < r1; r++)
+                    std::memcpy(padded.data() + (size_t)(r * Kp) * eb, wp + (size_t)(r * cols) * eb, (size_t)cols * eb);
+            });
+            wp = padded.data();
         }
+        if (lossless) return ep::encode_lossless(wp, Mp, Kp, rows, cols, p->container, threads, blob, blob_bytes);
         if (p->container < EP_C_BF16 || p->container > EP_C_INT8) return EP_ERR_INVALID_ARG;
         if (!(p->target_bpp > 0.f) || !std::isfinite(p->target_bpp)) return EP_ERR_INVALID_ARG;
         ep_params q = *p;
@@ -643,7 +691,7 @@ extern "C" ep_status ep_encode(const uint16_t* w, int64_t rows, int64_t cols, co
                 }
         });
         if (nonfinite) return EP_ERR_NONFINITE;
-        ep::LossyEncoder enc(w, rows, cols, q, threads);
+        ep::LossyEncoder enc(reinterpret_cast<const uint16_t*>(wp), Mp, Kp, rows, cols, q, threads);
         return enc.run(blob, blob_bytes);
     } catch (const std::bad_alloc&) {
         return EP_ERR_NOMEM;

@@ -1,5 +1,6 @@
 // Internal constants and the parsed stream layout of format version 1
-// (tile 32 x 128, 4 rANS lanes, 12-bit tables, 16-bit words).  Shared by
+// (tile 32 x 128, 4 rANS lanes, 12-bit tables, 16-bit words; any shape with
+// cols % 8 == 0, coded as the matrix padded with zeros to whole tiles).  Shared by
 // the host encoder, the host validator and the CUDA launchers.
 #pragma once
 
@@ -25,13 +26,23 @@ constexpr int kJMin = -640;
 constexpr int kJMax = 128;
 constexpr double kPeakBound = 15000.0;
 constexpr int kTileHeaderBytes = 24;   // 4 x u32 state + 4 x u16 word counts
-constexpr int kRawBytesPerTile = 4096;  // lossless: sign+mantissa byte per element
+constexpr int kRawBytesPerTile = 4096;  // lossless BF16/FP16: one sign+mantissa byte per element
+
+// Lossless element split (FORMAT.md §5): raw bytes per element kept uncoded
+// (BF16/FP16: 1, FP8: 0, FP32: 3) and element sizes in bytes.
+inline int lossless_raw_per_elem(int container) {
+    return container == EP_C_FP8_E4M3 ? 0 : (container == EP_C_FP32 ? 3 : 1);
+}
+inline bool lossless_container_ok(int c) {
+    return c == EP_C_BF16 || c == EP_C_FP16 || c == EP_C_FP8_E4M3 || c == EP_C_FP32;
+}
 
 // Stream layout after host validation.  All offsets are byte offsets from the
 // start of the blob.
 struct Layout {
     int mode = 0, container = 0, n_ctx = 0;
-    int64_t rows = 0, cols = 0, n_tiles = 0;
+    int64_t rows = 0, cols = 0, n_tiles = 0;  // true shape
+    int64_t rows_p = 0, cols_p = 0;           // tile grid: the shape padded to whole tiles
     float target_bpp = 0.f;
     int32_t j = 0;
     double delta = 0.0;
@@ -45,6 +56,8 @@ struct Layout {
 // per-tile word counts).  Returns EP_OK or EP_ERR_CORRUPT / EP_ERR_INVALID_ARG.
 ep_status parse_and_validate(const uint8_t* blob, size_t bytes, Layout* out);
 
-inline size_t container_bytes(int container) { return container >= EP_C_FP8_E4M3 ? 1 : 2; }
+inline size_t container_bytes(int container) {
+    return container == EP_C_FP32 ? 4 : (container >= EP_C_FP8_E4M3 ? 1 : 2);
+}
 
 }  // namespace ep

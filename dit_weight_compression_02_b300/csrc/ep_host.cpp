@@ -33,10 +33,13 @@ ep_status parse_and_validate(const uint8_t* b, size_t bytes, Layout* L) {
     L->target_bpp = rd<float>(b + 32);
     L->j = rd<int32_t>(b + 36);
     L->delta = rd<double>(b + 40);
-    if (L->mode > 1 || L->container > 3 || (L->mode == 1 && L->container != 0)) return EP_ERR_CORRUPT;
-    if (L->rows <= 0 || L->cols <= 0 || L->rows % kTileRows || L->cols % kTileCols) return EP_ERR_CORRUPT;
+    if (L->mode > 1 || (L->mode == 0 && L->container > 3) || (L->mode == 1 && !lossless_container_ok(L->container)))
+        return EP_ERR_CORRUPT;
+    if (L->rows <= 0 || L->cols <= 0 || L->cols % 8) return EP_ERR_CORRUPT;
     if (L->rows > (int64_t)1 << 40 || L->cols > (int64_t)1 << 40) return EP_ERR_CORRUPT;
-    if (L->n_tiles != (L->rows / kTileRows) * (L->cols / kTileCols)) return EP_ERR_CORRUPT;
+    L->rows_p = (L->rows + kTileRows - 1) / kTileRows * kTileRows;
+    L->cols_p = (L->cols + kTileCols - 1) / kTileCols * kTileCols;
+    if (L->n_tiles != (L->rows_p / kTileRows) * (L->cols_p / kTileCols)) return EP_ERR_CORRUPT;
     if (rd<uint16_t>(b + 48) != kTileRows || rd<uint16_t>(b + 50) != kTileCols || b[52] != kLanes) return EP_ERR_CORRUPT;
     L->n_ctx = b[53];
     if (L->n_ctx != (L->mode == 0 ? kLossyContexts : 1)) return EP_ERR_CORRUPT;
@@ -74,17 +77,18 @@ ep_status parse_and_validate(const uint8_t* b, size_t bytes, Layout* L) {
 
     // row metadata and tile offsets
     const uint64_t meta_floats =
-        L->mode == 1 ? 0 : (uint64_t)L->rows * (L->container >= EP_C_FP8_E4M3 ? 3u : 1u);
+        L->mode == 1 ? 0 : (uint64_t)L->rows_p * (L->container >= EP_C_FP8_E4M3 ? 3u : 1u);
     if (L->rowmeta_off + 4 * meta_floats > L->offsets_off) return EP_ERR_CORRUPT;
     if (L->offsets_off + 8ull * (uint64_t)(L->n_tiles + 1) > L->payload_off) return EP_ERR_CORRUPT;
     const uint64_t payload = L->total - L->payload_off;
-    const uint64_t min_tile = (L->mode == 1 ? (uint64_t)kRawBytesPerTile : 0u) + (uint64_t)kTileHeaderBytes;
+    const uint64_t raw_bytes = L->mode == 1 ? 4096u * (uint64_t)lossless_raw_per_elem(L->container) : 0u;
+    const uint64_t min_tile = raw_bytes + (uint64_t)kTileHeaderBytes;
     uint64_t prev = rd<uint64_t>(b + L->offsets_off);
     if (prev != 0) return EP_ERR_CORRUPT;
     for (int64_t t = 0; t < L->n_tiles; t++) {
         uint64_t nxt = rd<uint64_t>(b + L->offsets_off + 8ull * (uint64_t)(t + 1));
         if ((nxt & 15u) || nxt < prev + min_tile || nxt > payload) return EP_ERR_CORRUPT;
-        const uint8_t* th = b + L->payload_off + prev + (L->mode == 1 ? kRawBytesPerTile : 0);
+        const uint8_t* th = b + L->payload_off + prev + raw_bytes;
         uint64_t words = 0;
         for (int l = 0; l < kLanes; l++) words += rd<uint16_t>(th + 16 + 2 * l);
         if (min_tile + 2 * words > nxt - prev) return EP_ERR_CORRUPT;
@@ -104,7 +108,7 @@ const char* ep_status_string(ep_status s) {
     switch (s) {
         case EP_OK: return "ok";
         case EP_ERR_INVALID_ARG: return "invalid argument";
-        case EP_ERR_SHAPE: return "unsupported shape (rows % 32, cols % 128)";
+        case EP_ERR_SHAPE: return "unsupported shape (empty, or cols not a multiple of 8)";
         case EP_ERR_NONFINITE: return "non-finite input to a lossy encode";
         case EP_ERR_CORRUPT: return "corrupt stream";
         case EP_ERR_UNSUPPORTED: return "value range outside format version 1";

@@ -193,7 +193,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     uint4* dst = reinterpret_cast<uint4*>(yrow + col);
 #pragma unroll
-                    for (int i = 0; i < 4; i++) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+                    for (int i = 0; i < 4; i++)  // 8 columns each; N is a multiple of 8
+                        if (col + 8 * i < sh.N) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
                 }
             }
             tc_fence_before_sync();
@@ -282,7 +283,7 @@ ep_status check_gemm_args(const void* d_x, const void* d_w, const void* d_y, int
     if (!d_x || !d_w || !d_y || !d_status) return EP_ERR_INVALID_ARG;
     if (!aligned16(d_x) || !aligned16(d_w) || !aligned16(d_y)) return EP_ERR_INVALID_ARG;
     if (T <= 0 || N <= 0 || K <= 0) return EP_ERR_SHAPE;
-    if (N % 32 || K % 8) return EP_ERR_SHAPE;
+    if (N % 8 || K % 8) return EP_ERR_SHAPE;
     if (T > ((int64_t)1 << 31) - BM || N > ((int64_t)1 << 31) - BN || K > ((int64_t)1 << 31)) return EP_ERR_SHAPE;
     return EP_OK;
 }

@@ -19,7 +19,9 @@
  *
  * Conventions
  *  - Matrices are row-major; rows = out_features (M), cols = in_features (K).
- *    Version 1 needs rows % 32 == 0 and cols % 128 == 0.
+ *    Any rows >= 1 and cols >= 1 with cols % 8 == 0; the stream codes the
+ *    matrix padded with zeros to whole 32 x 128 tiles and the decoder writes
+ *    only the rows x cols values (row stride cols).
  *  - Every pointer is owned by the caller, except the blob returned by
  *    ep_encode (release it with ep_free).
  *  - Device entry points are asynchronous on `stream`; they allocate nothing
@@ -50,7 +52,7 @@ typedef struct CUstream_st *ep_stream_t;
 typedef enum {
     EP_OK = 0,
     EP_ERR_INVALID_ARG = 1, /* NULL pointer, misaligned pointer, bad enum, bad sizes */
-    EP_ERR_SHAPE = 2,       /* rows % 32 != 0 or cols % 128 != 0 or empty */
+    EP_ERR_SHAPE = 2,       /* empty, cols % 8 != 0, or a dimension above 2^40 */
     EP_ERR_NONFINITE = 3,   /* lossy input holds NaN or +-inf */
     EP_ERR_CORRUPT = 4,     /* stream fails validation (host) or decoding (device status) */
     EP_ERR_UNSUPPORTED = 5, /* value range outside format version 1 */
@@ -58,7 +60,9 @@ typedef enum {
     EP_ERR_CUDA = 7         /* a CUDA runtime call failed */
 } ep_status;
 
-typedef enum { EP_C_BF16 = 0, EP_C_FP16 = 1, EP_C_FP8_E4M3 = 2, EP_C_INT8 = 3 } ep_container;
+/* Containers of decoded weights.  Lossy streams: BF16, FP16, FP8 e4m3, INT8.
+ * Lossless streams keep the input's own type: BF16, FP16, FP8 e4m3 or FP32. */
+typedef enum { EP_C_BF16 = 0, EP_C_FP16 = 1, EP_C_FP8_E4M3 = 2, EP_C_INT8 = 3, EP_C_FP32 = 4 } ep_container;
 typedef enum { EP_MODE_LOSSY_E8 = 0, EP_MODE_LOSSLESS_TILEANS = 1 } ep_mode;
 
 /* Device status-word bits (OR-ed by the kernels). */
@@ -70,7 +74,8 @@ typedef enum { EP_MODE_LOSSY_E8 = 0, EP_MODE_LOSSLESS_TILEANS = 1 } ep_mode;
 typedef struct {
     int32_t mode;      /* ep_mode */
     float target_bpp;  /* lossy: target coded bits per parameter (> 0) */
-    int32_t container; /* ep_container of the decoded weights (lossless: EP_C_BF16) */
+    int32_t container; /* ep_container of the decoded weights; lossless: the input's type
+                          (EP_C_BF16, EP_C_FP16, EP_C_FP8_E4M3 or EP_C_FP32) */
     float sample_frac; /* fraction of rows sampled by the rate search; <= 0 selects 0.05 */
     int32_t n_threads; /* host threads for ep_encode; <= 0 selects all hardware threads */
 } ep_params;
@@ -84,7 +89,7 @@ typedef struct {
     uint64_t total_bytes;
     uint32_t n_sample_rows;
     double actual_bpp;   /* 8 * total_bytes / (rows * cols): includes every byte of metadata */
-    size_t out_elem_bytes; /* bytes per decoded element (2 for BF16/FP16, 1 for FP8/INT8) */
+    size_t out_elem_bytes; /* bytes per decoded element (2 for BF16/FP16, 1 for FP8/INT8, 4 for FP32) */
     int32_t has_row_scale; /* 1 when ep_decode also writes per-row output scales t_r */
 } ep_info;
 
@@ -93,16 +98,19 @@ int32_t ep_version(void);
 const char *ep_status_string(ep_status s);
 
 /*
- * Host encoder.  w_bf16: rows x cols BF16 bit patterns (host memory).
+ * Host encoder.  w: rows x cols elements, row-major, in host memory: BF16
+ * bit patterns for lossy streams; for lossless streams elements of the type
+ * p->container names (2 bytes for BF16/FP16, 1 for FP8 e4m3, 4 for FP32).
  * Lossy (p->mode == EP_MODE_LOSSY_E8): row-normalised E8 quantisation at the
  * resolution whose sampled rate estimate is closest to p->target_bpp, then
- * 12-bit rANS in 4-lane tiles of 32 x 128.  Lossless: exponent byte coded,
- * sign+mantissa raw; decoding restores every bit.
+ * 12-bit rANS in 4-lane tiles of 32 x 128.  Lossless: the exponent byte
+ * (FP8: the whole element) is coded, sign and mantissa stored raw; decoding
+ * restores every bit.
  * On success *blob points to *blob_bytes bytes allocated by the library
  * (release with ep_free).  Errors: EP_ERR_INVALID_ARG, EP_ERR_SHAPE,
  * EP_ERR_NONFINITE (lossy only), EP_ERR_UNSUPPORTED, EP_ERR_NOMEM.
  */
-ep_status ep_encode(const uint16_t *w_bf16, int64_t rows, int64_t cols, const ep_params *p, uint8_t **blob,
+ep_status ep_encode(const void *w, int64_t rows, int64_t cols, const ep_params *p, uint8_t **blob,
                     size_t *blob_bytes);
 void ep_free(void *p);
 
@@ -166,7 +174,7 @@ typedef struct {
 
 typedef struct {
     int64_t n_items, total_units; /* total_units: work units (32 tile groups) of all items */
-    int32_t ring, kind, n_ctx, reserved;
+    int32_t ring, kind, n_ctx, reserved; /* reserved: set when an item's shape is not whole tiles */
     void *d_workspace;
     size_t workspace_bytes;
     uint64_t items_off, units_off, counters_off;
@@ -183,7 +191,7 @@ ep_status ep_batch_decode(const ep_batch_plan *plan, uint32_t *d_status, ep_stre
  * BF16 X [tokens x cols], W [rows x cols] and Y [tokens x rows]; the product
  * is accumulated in fp32 by tcgen05 tensor-core instructions and rounded to
  * BF16 once.  Device pointers are caller-owned and 16-byte aligned; tokens
- * may be any positive count, rows must be a multiple of 32 and cols of 8.
+ * may be any positive count, rows and cols must be multiples of 8.
  * d_status (one u32) is zeroed by the call; the kernel sets
  * EP_STATUS_WAIT_TIMEOUT if an internal pipeline wait gives up (about 2 s),
  * which never happens in a correct run.  Returns EP_OK once enqueued.
@@ -199,7 +207,7 @@ ep_status ep_linear_bf16(const uint16_t *d_x, const uint16_t *d_w, uint16_t *d_y
 
 /*
  * CompressedLinear forward on a lossy BF16 stream (h_blob / d_blob as for
- * ep_decode; rows = out_features, cols = in_features).  mode
+ * ep_decode; rows = out_features, cols = in_features; both multiples of 8).  mode
  * EP_LINEAR_DECODE_THEN_GEMM needs d_ws of at least rows * cols * 2 bytes.
  * Stream corruption found by the decoder shows up in d_status like
  * ep_decode's.  Errors before launch: EP_ERR_INVALID_ARG, EP_ERR_SHAPE,

@@ -91,6 +91,8 @@ def lib():
         L.oracle_encode.argtypes = [P, i64, i64, f32, i32, f32, P, P]
         L.oracle_encode_lossless.restype = i32
         L.oracle_encode_lossless.argtypes = [P, i64, i64, P, P]
+        L.oracle_encode_lossless_dtype.restype = i32
+        L.oracle_encode_lossless_dtype.argtypes = [P, i64, i64, i32, P, P]
         L.oracle_free.argtypes = [P]
         L.oracle_decode.restype = i32
         L.oracle_decode.argtypes = [P, sz, P, P, i64, i64]
@@ -229,12 +231,17 @@ def encode(w_bits: np.ndarray, target_bpp: float = 4.0, container: str = "bf16",
     return _take_blob(ptr, size)
 
 
-def encode_lossless(w_bits: np.ndarray) -> bytes:
-    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+LOSSLESS_DTYPES = {"bf16": (0, np.uint16), "fp16": (1, np.uint16), "fp8": (2, np.uint8), "fp32": (4, np.uint32)}
+
+
+def encode_lossless(w_bits: np.ndarray, dtype: str = "bf16") -> bytes:
+    """Lossless tiled ANS of a matrix of element bit patterns (uint16 for BF16/FP16, uint8 for FP8, uint32 for FP32)."""
+    code, npt = LOSSLESS_DTYPES[dtype]
+    w_bits = np.ascontiguousarray(w_bits, dtype=npt)
     ptr = ctypes.c_void_p(0)
     size = ctypes.c_size_t(0)
-    rc = lib().oracle_encode_lossless(_p(w_bits), w_bits.shape[0], w_bits.shape[1], ctypes.byref(ptr),
-                                      ctypes.byref(size))
+    rc = lib().oracle_encode_lossless_dtype(_p(w_bits), w_bits.shape[0], w_bits.shape[1], code, ctypes.byref(ptr),
+                                            ctypes.byref(size))
     if rc:
         raise OracleError(rc, "encode_lossless")
     return _take_blob(ptr, size)
@@ -253,7 +260,7 @@ def header(blob: bytes) -> dict:
     }
 
 
-_OUT_DTYPE = {0: np.uint16, 1: np.uint16, 2: np.uint8, 3: np.int8}
+_OUT_DTYPE = {0: np.uint16, 1: np.uint16, 2: np.uint8, 3: np.int8, 4: np.uint32}
 
 
 def decode(blob: bytes, t_lo: int = 0, t_hi: int | None = None, out=None):

@@ -12,7 +12,43 @@
 
 enum { O_OK = 0, O_ERR_ARG = 1, O_ERR_SHAPE = 2, O_ERR_NONFINITE = 3, O_ERR_CORRUPT = 4, O_ERR_UNSUPPORTED = 5,
        O_ERR_NOMEM = 6 };
-enum { O_C_BF16 = 0, O_C_FP16 = 1, O_C_FP8 = 2, O_C_INT8 = 3 };
+enum { O_C_BF16 = 0, O_C_FP16 = 1, O_C_FP8 = 2, O_C_INT8 = 3, O_C_FP32 = 4 };
+
+/* ---------------------------------------------- lossless element split (§5)
+   BF16 / FP16: coded byte = bits 14..7, raw byte = bit 15 | bits 6..0
+   FP8 e4m3:    coded byte = the element, no raw byte
+   FP32:        coded byte = bits 30..23 (the exponent), raw bytes =
+                (bit 31 | bits 22..16), bits 15..8, bits 7..0 */
+static int lossless_dtype_ok(int c) { return c == O_C_BF16 || c == O_C_FP16 || c == O_C_FP8 || c == O_C_FP32; }
+static int elem_bytes(int c) { return c == O_C_FP8 ? 1 : (c == O_C_FP32 ? 4 : 2); }
+static int raw_per_elem(int c) { return c == O_C_FP8 ? 0 : (c == O_C_FP32 ? 3 : 1); }
+
+static uint8_t split_elem(int c, const uint8_t *x, uint8_t *raw) {
+    if (c == O_C_FP8) return x[0];
+    if (c == O_C_FP32) {
+        uint32_t v = (uint32_t)x[0] | ((uint32_t)x[1] << 8) | ((uint32_t)x[2] << 16) | ((uint32_t)x[3] << 24);
+        raw[0] = (uint8_t)(((v >> 24) & 0x80) | ((v >> 16) & 0x7F));
+        raw[1] = (uint8_t)(v >> 8);
+        raw[2] = (uint8_t)v;
+        return (uint8_t)(v >> 23);
+    }
+    uint16_t v = (uint16_t)(x[0] | (x[1] << 8));
+    raw[0] = (uint8_t)(((v >> 8) & 0x80) | (v & 0x7F));
+    return (uint8_t)(v >> 7);
+}
+
+static void join_elem(int c, uint8_t e, const uint8_t *raw, uint8_t *x) {
+    if (c == O_C_FP8) { x[0] = e; return; }
+    if (c == O_C_FP32) {
+        uint32_t v = ((uint32_t)(raw[0] & 0x80) << 24) | ((uint32_t)e << 23) | ((uint32_t)(raw[0] & 0x7F) << 16) |
+                     ((uint32_t)raw[1] << 8) | raw[2];
+        for (int i = 0; i < 4; i++) x[i] = (uint8_t)(v >> (8 * i));
+        return;
+    }
+    uint16_t v = (uint16_t)(((raw[0] & 0x80) << 8) | ((uint16_t)e << 7) | (raw[0] & 0x7F));
+    x[0] = (uint8_t)v;
+    x[1] = (uint8_t)(v >> 8);
+}
 
 #define TILE_R 32
 #define TILE_C 128
@@ -37,6 +73,17 @@ static uint16_t get_u16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)
 static uint32_t get_u32(const uint8_t *p) { uint32_t v = 0; for (int i = 3; i >= 0; i--) v = (v << 8) | p[i]; return v; }
 static uint64_t get_u64(const uint8_t *p) { uint64_t v = 0; for (int i = 7; i >= 0; i--) v = (v << 8) | p[i]; return v; }
 static uint64_t align16(uint64_t v) { return (v + 15u) & ~(uint64_t)15u; }
+/* tile-grid dimensions: the matrix is padded with zeros to whole tiles (FORMAT §1) */
+static int64_t pad_rows(int64_t M) { return (M + TILE_R - 1) / TILE_R * TILE_R; }
+static int64_t pad_cols(int64_t K) { return (K + TILE_C - 1) / TILE_C * TILE_C; }
+
+/* zero-padded copy of w (M x K) as Mp x Kp; NULL when out of memory */
+static uint16_t *padded_copy(const uint16_t *w, int64_t M, int64_t K, int64_t Mp, int64_t Kp) {
+    uint16_t *wp = (uint16_t *)calloc((size_t)(Mp * Kp), sizeof(uint16_t));
+    if (!wp) return NULL;
+    for (int64_t r = 0; r < M; r++) memcpy(wp + r * Kp, w + r * K, (size_t)K * sizeof(uint16_t));
+    return wp;
+}
 
 double oracle_bf16_to_f64(uint16_t b) {
     uint32_t u = (uint32_t)b << 16;
@@ -325,21 +372,23 @@ int8_t oracle_f32_to_int8(float v) {
 
 /* ---------------------------------------------------- quantisation pass */
 typedef struct {
-    int64_t M, K;
-    double *s;    /* row RMS */
-    double *peak; /* row max |w| */
+    int64_t M, K;   /* true shape */
+    int64_t Mp, Kp; /* padded shape of the matrix the stats index (row stride Kp) */
+    double *s;      /* row RMS over the K true columns (0 for padding rows) */
+    double *peak;   /* row max |w| */
 } rowstats;
 
-static int row_stats(const uint16_t *w, int64_t M, int64_t K, rowstats *rs) {
-    rs->M = M; rs->K = K;
-    rs->s = (double *)malloc((size_t)M * sizeof(double));
-    rs->peak = (double *)malloc((size_t)M * sizeof(double));
+/* wp: the zero-padded Mp x Kp matrix; statistics of row r use its K true columns */
+static int row_stats(const uint16_t *wp, int64_t M, int64_t K, int64_t Mp, int64_t Kp, rowstats *rs) {
+    rs->M = M; rs->K = K; rs->Mp = Mp; rs->Kp = Kp;
+    rs->s = (double *)calloc((size_t)Mp, sizeof(double));
+    rs->peak = (double *)calloc((size_t)Mp, sizeof(double));
     if (!rs->s || !rs->peak) return O_ERR_NOMEM;
     for (int64_t r = 0; r < M; r++) {
-        rs->s[r] = oracle_row_rms(w + r * K, K);
+        rs->s[r] = oracle_row_rms(wp + r * Kp, K);
         double pk = 0.0;
         for (int64_t k = 0; k < K; k++) {
-            double v = fabs(oracle_bf16_to_f64(w[r * K + k]));
+            double v = fabs(oracle_bf16_to_f64(wp[r * Kp + k]));
             if (v > pk) pk = v;
         }
         rs->peak[r] = pk;
@@ -389,8 +438,9 @@ static int64_t n_sample_rows(int64_t M, float sample_frac) {
     return n;
 }
 
-static double estimate_with_stats(const uint16_t *w, const rowstats *rs, float sample_frac, int j) {
-    int64_t M = rs->M, K = rs->K;
+/* wp: the zero-padded matrix (row stride rs->Kp); only true rows and columns are sampled */
+static double estimate_with_stats(const uint16_t *wp, const rowstats *rs, float sample_frac, int j) {
+    int64_t M = rs->M, K = rs->K, Kp = rs->Kp;
     int64_t ns = n_sample_rows(M, sample_frac);
     uint64_t counts[N_CTX_LOSSY][256];
     memset(counts, 0, sizeof(counts));
@@ -403,7 +453,7 @@ static double estimate_with_stats(const uint16_t *w, const rowstats *rs, float s
             int c;
             uint8_t u[8], cx[8];
             int32_t pl[8];
-            quantise_block(w, K, r, col0, g, a, &c);
+            quantise_block(wp, Kp, r, col0, g, a, &c);
             n_esc += (uint64_t)oracle_block_symbols(a, c, u, cx, pl);
             for (int k = 0; k < 8; k++) counts[cx[k]][u[k]]++;
         }
@@ -419,10 +469,14 @@ static double estimate_with_stats(const uint16_t *w, const rowstats *rs, float s
 }
 
 double oracle_estimate_bpp(const uint16_t *w, int64_t M, int64_t K, float sample_frac, int j) {
+    if (M <= 0 || K <= 0 || K % 8) return -1.0;
+    int64_t Mp = pad_rows(M), Kp = pad_cols(K);
+    uint16_t *wp = padded_copy(w, M, K, Mp, Kp);
     rowstats rs;
-    if (row_stats(w, M, K, &rs) != O_OK) { free_stats(&rs); return -1.0; }
-    double e = estimate_with_stats(w, &rs, sample_frac, j);
-    free_stats(&rs);
+    double e = -1.0;
+    if (wp && row_stats(wp, M, K, Mp, Kp, &rs) == O_OK) e = estimate_with_stats(wp, &rs, sample_frac, j);
+    if (wp) free_stats(&rs);
+    free(wp);
     return e;
 }
 
@@ -444,10 +498,14 @@ static int select_with_stats(const uint16_t *w, const rowstats *rs, float target
 }
 
 int oracle_select_j(const uint16_t *w, int64_t M, int64_t K, float target_bpp, float sample_frac, int *j_lo_out) {
+    if (M <= 0 || K <= 0 || K % 8) return J_MAX + 1;
+    int64_t Mp = pad_rows(M), Kp = pad_cols(K);
+    uint16_t *wp = padded_copy(w, M, K, Mp, Kp);
     rowstats rs;
-    if (row_stats(w, M, K, &rs) != O_OK) { free_stats(&rs); return J_MAX + 1; }
-    int j = select_with_stats(w, &rs, target_bpp, sample_frac, j_lo_out);
-    free_stats(&rs);
+    int j = J_MAX + 1;
+    if (wp && row_stats(wp, M, K, Mp, Kp, &rs) == O_OK) j = select_with_stats(wp, &rs, target_bpp, sample_frac, j_lo_out);
+    if (wp) free_stats(&rs);
+    free(wp);
     return j;
 }
 
@@ -527,9 +585,9 @@ static int serialise(const blob_parts *bp, uint8_t **blob, size_t *bytes) {
 }
 
 /* one tile's payload from its lanes' (raw?, states, words) */
-static int pack_tile(const uint8_t *raw, const uint32_t state[4], uint16_t *const words[4], const int64_t nw[4],
-                     uint8_t **out, uint64_t *size) {
-    uint64_t n = (raw ? 4096 : 0) + 16 + 8;
+static int pack_tile(const uint8_t *raw, uint64_t raw_len, const uint32_t state[4], uint16_t *const words[4],
+                     const int64_t nw[4], uint8_t **out, uint64_t *size) {
+    uint64_t n = (raw ? raw_len : 0) + 16 + 8;
     for (int l = 0; l < 4; l++) {
         if (nw[l] > 65535) return O_ERR_UNSUPPORTED;
         n += 2 * (uint64_t)nw[l];
@@ -537,7 +595,7 @@ static int pack_tile(const uint8_t *raw, const uint32_t state[4], uint16_t *cons
     n = align16(n);
     uint8_t *t = (uint8_t *)calloc((size_t)n, 1), *p = t;
     if (!t) return O_ERR_NOMEM;
-    if (raw) { memcpy(p, raw, 4096); p += 4096; }
+    if (raw) { memcpy(p, raw, (size_t)raw_len); p += raw_len; }
     for (int l = 0; l < 4; l++) { put_u32(p, state[l]); p += 4; }
     for (int l = 0; l < 4; l++) { put_u16(p, (uint16_t)nw[l]); p += 2; }
     for (int l = 0; l < 4; l++)
@@ -557,15 +615,25 @@ static void free_tiles(uint8_t **tb, int64_t n) {
 int oracle_encode(const uint16_t *w, int64_t M, int64_t K, float target_bpp, int container, float sample_frac,
                   uint8_t **blob, size_t *bytes) {
     if (!w || !blob || !bytes) return O_ERR_ARG;
-    if (M <= 0 || K <= 0 || M % TILE_R || K % TILE_C) return O_ERR_SHAPE;
+    if (M <= 0 || K <= 0 || K % 8) return O_ERR_SHAPE;
     if (container < O_C_BF16 || container > O_C_INT8) return O_ERR_ARG;
     if (!(target_bpp > 0.0f) || !isfinite(target_bpp) || !(sample_frac > 0.0f) || !isfinite(sample_frac)) return O_ERR_ARG;
     for (int64_t i = 0; i < M * K; i++)
         if ((w[i] & 0x7F80) == 0x7F80) return O_ERR_NONFINITE;
 
+    /* from here on the matrix is the zero-padded Mp x Kp one; the true shape
+       only enters the row statistics, the rate estimate and the header */
+    const int64_t M_true = M, K_true = K;
+    const uint16_t *w_true = w;
+    M = pad_rows(M_true);
+    K = pad_cols(K_true);
+    uint16_t *wp = padded_copy(w_true, M_true, K_true, M, K);
+    if (!wp) return O_ERR_NOMEM;
+    w = wp;
+
     rowstats rs;
-    int rc = row_stats(w, M, K, &rs);
-    if (rc != O_OK) { free_stats(&rs); return rc; }
+    int rc = row_stats(w, M_true, K_true, M, K, &rs);
+    if (rc != O_OK) { free_stats(&rs); free(wp); return rc; }
     int j = select_with_stats(w, &rs, target_bpp, sample_frac, NULL);
 
     int64_t n_blocks = M * (K / 8);
@@ -609,9 +677,9 @@ int oracle_encode(const uint16_t *w, int64_t M, int64_t K, float target_bpp, int
     blob_parts bp;
     memset(&bp, 0, sizeof(bp));
     bp.mode = 0; bp.container = container; bp.n_ctx = N_CTX_LOSSY;
-    bp.M = M; bp.K = K; bp.n_tiles = (M / TILE_R) * (K / TILE_C);
+    bp.M = M_true; bp.K = K_true; bp.n_tiles = (M / TILE_R) * (K / TILE_C);
     bp.target_bpp = target_bpp; bp.j = j; bp.delta = oracle_delta(j);
-    bp.n_sample = (uint32_t)n_sample_rows(M, sample_frac);
+    bp.n_sample = (uint32_t)n_sample_rows(M_true, sample_frac);
     for (int c = 0; c < N_CTX_LOSSY; c++) oracle_normalize(counts[c], bp.freq[c]);
     for (int u = 0; u < 256; u++) bp.freq[CTX_UNIFORM][u] = 16;
 
@@ -662,7 +730,7 @@ int oracle_encode(const uint16_t *w, int64_t M, int64_t K, float target_bpp, int
             }
             rc = oracle_rans_encode(ls, lc, n, &bp.freq[0][0], &state[l], lw[l], max_syms, &nw[l]);
         }
-        if (rc == O_OK) rc = pack_tile(NULL, state, lw, nw, &bp.tile_bytes[tile], &bp.tile_size[tile]);
+        if (rc == O_OK) rc = pack_tile(NULL, 0, state, lw, nw, &bp.tile_bytes[tile], &bp.tile_size[tile]);
     }
     if (rc == O_OK) rc = serialise(&bp, blob, bytes);
 done:
@@ -674,42 +742,55 @@ done:
 done_early:
     free(val); free(sym); free(cos_); free(meta);
     free_stats(&rs);
+    free(wp);
     return rc;
 }
 
 /* ------------------------------------------------------ lossless encoder (§5) */
-int oracle_encode_lossless(const uint16_t *w, int64_t M, int64_t K, uint8_t **blob, size_t *bytes) {
-    if (!w || !blob || !bytes) return O_ERR_ARG;
-    if (M <= 0 || K <= 0 || M % TILE_R || K % TILE_C) return O_ERR_SHAPE;
+int oracle_encode_lossless_dtype(const void *w_in, int64_t M, int64_t K, int dtype, uint8_t **blob, size_t *bytes) {
+    if (!w_in || !blob || !bytes) return O_ERR_ARG;
+    if (!lossless_dtype_ok(dtype)) return O_ERR_ARG;
+    if (M <= 0 || K <= 0 || K % 8) return O_ERR_SHAPE;
+    const int eb = elem_bytes(dtype), rb = raw_per_elem(dtype);
+    /* the zero-padded Mp x Kp matrix is coded; the header keeps the true shape */
+    const int64_t M_true = M, K_true = K;
+    M = pad_rows(M_true);
+    K = pad_cols(K_true);
+    uint8_t *w = (uint8_t *)calloc((size_t)(M * K), (size_t)eb);
+    if (!w) return O_ERR_NOMEM;
+    for (int64_t r = 0; r < M_true; r++)
+        memcpy(w + (size_t)(r * K) * eb, (const uint8_t *)w_in + (size_t)(r * K_true) * eb, (size_t)K_true * eb);
     uint64_t counts[256];
     memset(counts, 0, sizeof(counts));
-    for (int64_t i = 0; i < M * K; i++) counts[(w[i] >> 7) & 0xFF]++;
+    uint8_t scratch[3];
+    for (int64_t i = 0; i < M * K; i++) counts[split_elem(dtype, w + (size_t)i * eb, scratch)]++;
     blob_parts bp;
     memset(&bp, 0, sizeof(bp));
-    bp.mode = 1; bp.container = O_C_BF16; bp.n_ctx = 1;
-    bp.M = M; bp.K = K; bp.n_tiles = (M / TILE_R) * (K / TILE_C);
+    bp.mode = 1; bp.container = dtype; bp.n_ctx = 1;
+    bp.M = M_true; bp.K = K_true; bp.n_tiles = (M / TILE_R) * (K / TILE_C);
     oracle_normalize(counts, bp.freq[0]);
     float dummy = 0.0f;
     bp.rowmeta = &dummy;
     bp.rowmeta_floats = 0;
     bp.tile_bytes = (uint8_t **)calloc((size_t)bp.n_tiles, sizeof(uint8_t *));
     bp.tile_size = (uint64_t *)calloc((size_t)bp.n_tiles, sizeof(uint64_t));
-    uint8_t raw[4096], ls[1024], lc[1024];
+    const uint64_t raw_len = (uint64_t)rb * 4096u;
+    uint8_t *raw = (uint8_t *)malloc(raw_len ? raw_len : 1);
+    uint8_t ls[1024], lc[1024];
     uint16_t *lw[4];
     int rc = O_OK;
     for (int l = 0; l < 4; l++) lw[l] = (uint16_t *)malloc(sizeof(uint16_t) * 1024);
-    if (!bp.tile_bytes || !bp.tile_size || !lw[0] || !lw[1] || !lw[2] || !lw[3]) rc = O_ERR_NOMEM;
+    if (!raw || !bp.tile_bytes || !bp.tile_size || !lw[0] || !lw[1] || !lw[2] || !lw[3]) rc = O_ERR_NOMEM;
     memset(lc, 0, sizeof(lc));
     int64_t tiles_per_row = K / TILE_C;
     for (int64_t tile = 0; tile < bp.n_tiles && rc == O_OK; tile++) {
         int64_t r0 = (tile / tiles_per_row) * TILE_R, c0 = (tile % tiles_per_row) * TILE_C;
+        /* raw bytes in block order: element i of block b at rb * (8 b + i) */
         for (int b = 0; b < BLOCKS_PER_TILE; b++) {
             int br, bc;
             block_place(b, &br, &bc);
-            for (int i = 0; i < 8; i++) {
-                uint16_t x = w[(r0 + br) * K + c0 + bc + i];
-                raw[8 * b + i] = (uint8_t)(((x >> 8) & 0x80) | (x & 0x7F));
-            }
+            for (int i = 0; i < 8; i++)
+                split_elem(dtype, w + (size_t)((r0 + br) * K + c0 + bc + i) * eb, raw + (size_t)rb * (8 * b + i));
         }
         uint32_t state[4];
         int64_t nw[4];
@@ -718,17 +799,24 @@ int oracle_encode_lossless(const uint16_t *w, int64_t M, int64_t K, uint8_t **bl
             for (int b = l; b < BLOCKS_PER_TILE; b += 4) {
                 int br, bc;
                 block_place(b, &br, &bc);
-                for (int i = 0; i < 8; i++) ls[n++] = (uint8_t)((w[(r0 + br) * K + c0 + bc + i] >> 7) & 0xFF);
+                for (int i = 0; i < 8; i++)
+                    ls[n++] = split_elem(dtype, w + (size_t)((r0 + br) * K + c0 + bc + i) * eb, scratch);
             }
             rc = oracle_rans_encode(ls, lc, n, &bp.freq[0][0], &state[l], lw[l], 1024, &nw[l]);
         }
-        if (rc == O_OK) rc = pack_tile(raw, state, lw, nw, &bp.tile_bytes[tile], &bp.tile_size[tile]);
+        if (rc == O_OK) rc = pack_tile(rb ? raw : NULL, raw_len, state, lw, nw, &bp.tile_bytes[tile], &bp.tile_size[tile]);
     }
     if (rc == O_OK) rc = serialise(&bp, blob, bytes);
     for (int l = 0; l < 4; l++) free(lw[l]);
     free_tiles(bp.tile_bytes, bp.n_tiles);
     free(bp.tile_size);
+    free(raw);
+    free(w);
     return rc;
+}
+
+int oracle_encode_lossless(const uint16_t *w, int64_t M, int64_t K, uint8_t **blob, size_t *bytes) {
+    return oracle_encode_lossless_dtype(w, M, K, O_C_BF16, blob, bytes);
 }
 
 void oracle_free(void *p) { free(p); }
@@ -736,7 +824,8 @@ void oracle_free(void *p) { free(p); }
 /* ---------------------------------------------------------------- decoder */
 typedef struct {
     int mode, container, n_ctx;
-    int64_t M, K, n_tiles;
+    int64_t M, K, n_tiles; /* true shape */
+    int64_t Mp, Kp;        /* tile grid: the shape padded to whole tiles */
     uint64_t rowmeta_off, offsets_off, payload_off;
     uint32_t freq[8][256], cum[8][256];
     int16_t tab[8][PROB_SCALE];
@@ -750,9 +839,13 @@ static int parse(const uint8_t *b, size_t bytes, parsed *ps) {
     ps->M = (int64_t)get_u64(b + 8);
     ps->K = (int64_t)get_u64(b + 16);
     ps->n_tiles = (int64_t)get_u64(b + 24);
-    if (ps->mode > 1 || ps->container > 3 || (ps->mode == 1 && ps->container != 0)) return O_ERR_CORRUPT;
-    if (ps->M <= 0 || ps->K <= 0 || ps->M % TILE_R || ps->K % TILE_C) return O_ERR_CORRUPT;
-    if (ps->n_tiles != (ps->M / TILE_R) * (ps->K / TILE_C)) return O_ERR_CORRUPT;
+    if (ps->mode > 1 || (ps->mode == 0 && ps->container > 3) || (ps->mode == 1 && !lossless_dtype_ok(ps->container)))
+        return O_ERR_CORRUPT;
+    if (ps->M <= 0 || ps->K <= 0 || ps->K % 8) return O_ERR_CORRUPT;
+    if (ps->M > ((int64_t)1 << 40) || ps->K > ((int64_t)1 << 40)) return O_ERR_CORRUPT;
+    ps->Mp = pad_rows(ps->M);
+    ps->Kp = pad_cols(ps->K);
+    if (ps->n_tiles != (ps->Mp / TILE_R) * (ps->Kp / TILE_C)) return O_ERR_CORRUPT;
     if (get_u16(b + 48) != TILE_R || get_u16(b + 50) != TILE_C || b[52] != LANES) return O_ERR_CORRUPT;
     ps->n_ctx = b[53];
     if (ps->n_ctx != (ps->mode == 0 ? N_CTX_LOSSY : 1)) return O_ERR_CORRUPT;
@@ -779,10 +872,10 @@ static int parse(const uint8_t *b, size_t bytes, parsed *ps) {
     }
     if (ps->mode == 0)
         for (int u = 0; u < 256; u++) ps->freq[CTX_UNIFORM][u] = 16;
-    uint64_t meta_floats = ps->mode == 1 ? 0 : (uint64_t)ps->M * ((ps->container >= O_C_FP8) ? 3 : 1);
+    uint64_t meta_floats = ps->mode == 1 ? 0 : (uint64_t)ps->Mp * ((ps->container >= O_C_FP8) ? 3 : 1);
     if (ps->rowmeta_off + 4 * meta_floats > ps->offsets_off) return O_ERR_CORRUPT;
     if (ps->offsets_off + 8 * (uint64_t)(ps->n_tiles + 1) > ps->payload_off) return O_ERR_CORRUPT;
-    uint64_t prev = 0, min_tile = (ps->mode == 1 ? 4096u : 0u) + 24u;
+    uint64_t prev = 0, min_tile = (ps->mode == 1 ? 4096u * (uint64_t)raw_per_elem(ps->container) : 0u) + 24u;
     for (int64_t t = 0; t <= ps->n_tiles; t++) {
         uint64_t o = get_u64(b + ps->offsets_off + 8 * (uint64_t)t);
         if (t == 0 && o != 0) return O_ERR_CORRUPT;
@@ -800,19 +893,22 @@ static int parse(const uint8_t *b, size_t bytes, parsed *ps) {
 
 static float rowmeta_at(const uint8_t *b, const parsed *ps, int which, int64_t r) {
     float v;
-    memcpy(&v, b + ps->rowmeta_off + 4 * ((uint64_t)which * (uint64_t)ps->M + (uint64_t)r), 4);
+    memcpy(&v, b + ps->rowmeta_off + 4 * ((uint64_t)which * (uint64_t)ps->Mp + (uint64_t)r), 4);
     return v;
 }
 
-/* decode one tile; writes container values (out) and/or symbol bytes (sym_out) */
+/* decode one tile; writes container values (out) and/or symbol bytes (sym_out)
+   for the blocks inside the true M x K matrix (padding blocks are decoded and
+   checked, not written) */
 static int decode_tile(const uint8_t *b, const parsed *ps, int64_t tile, void *out, uint8_t *sym_out, int32_t *k_out) {
-    int64_t K = ps->K, tiles_per_row = K / TILE_C;
+    int64_t K = ps->K, tiles_per_row = ps->Kp / TILE_C;
     int64_t r0 = (tile / tiles_per_row) * TILE_R, c0 = (tile % tiles_per_row) * TILE_C;
     uint64_t t_off = get_u64(b + ps->offsets_off + 8 * (uint64_t)tile);
     uint64_t t_end = get_u64(b + ps->offsets_off + 8 * (uint64_t)(tile + 1));
     const uint8_t *tp = b + ps->payload_off + t_off;
     const uint8_t *raw = NULL;
-    if (ps->mode == 1) { raw = tp; tp += 4096; }
+    const int rb = ps->mode == 1 ? raw_per_elem(ps->container) : 0, eb = elem_bytes(ps->container);
+    if (ps->mode == 1) { raw = tp; tp += 4096 * rb; }
     uint32_t state[4];
     int64_t nw[4];
     for (int l = 0; l < 4; l++) state[l] = get_u32(tp + 4 * l);
@@ -831,14 +927,14 @@ static int decode_tile(const uint8_t *b, const parsed *ps, int64_t tile, void *o
             int br, bc;
             block_place(bb, &br, &bc);
             int64_t r = r0 + br, col0 = c0 + bc;
+            int inside = r < ps->M && col0 < ps->K;
             if (ps->mode == 1) {
                 for (int i = 0; i < 8; i++) {
                     int e = lane_symbol(&d, ps->freq[0], ps->cum[0], ps->tab[0]);
-                    uint8_t rw = raw[8 * bb + i];
-                    if (sym_out) sym_out[r * K + col0 + i] = (uint8_t)e;
-                    if (out)
-                        ((uint16_t *)out)[r * K + col0 + i] =
-                            (uint16_t)(((rw & 0x80) << 8) | ((uint16_t)e << 7) | (rw & 0x7F));
+                    if (sym_out && inside) sym_out[r * K + col0 + i] = (uint8_t)e;
+                    if (out && inside)
+                        join_elem(ps->container, (uint8_t)e, raw + (size_t)rb * (8 * bb + i),
+                                  (uint8_t *)out + (size_t)(r * K + col0 + i) * eb);
                 }
                 continue;
             }
@@ -864,11 +960,11 @@ static int decode_tile(const uint8_t *b, const parsed *ps, int64_t tile, void *o
             for (int i = 0; i < 7; i++) { a[i] = (v[i] - c) / 2; sum7 += a[i]; }
             int64_t p = sum7 & 1;
             a[7] = 2 * ((v[7] - c) / 4) + p;
-            if (sym_out)
+            if (sym_out && inside)
                 for (int i = 0; i < 8; i++) sym_out[r * K + col0 + i] = (uint8_t)u[i];
-            if (k_out)
+            if (k_out && inside)
                 for (int i = 0; i < 8; i++) k_out[r * K + col0 + i] = (int32_t)(2 * a[i] + c);
-            if (!out) continue;
+            if (!out || !inside) continue;
             float g = rowmeta_at(b, ps, 0, r);
             float m = (ps->container >= O_C_FP8) ? rowmeta_at(b, ps, 1, r) : 1.0f;
             for (int i = 0; i < 8; i++) {
@@ -943,3 +1039,4 @@ void oracle_gemm_f64(const double *x, const double *w, double *y, int64_t T, int
             y[t * N + n] = s;
         }
 }
+

@@ -62,6 +62,8 @@ int oracle_select_j(const uint16_t *w, int64_t M, int64_t K, float target_bpp, f
 int oracle_encode(const uint16_t *w, int64_t M, int64_t K, float target_bpp, int container, float sample_frac,
                   uint8_t **blob, size_t *bytes);
 int oracle_encode_lossless(const uint16_t *w, int64_t M, int64_t K, uint8_t **blob, size_t *bytes);
+/* lossless tiled ANS of BF16 (0), FP16 (1), FP8 e4m3 (2) or FP32 (4) elements (FORMAT §5) */
+int oracle_encode_lossless_dtype(const void *w, int64_t M, int64_t K, int dtype, uint8_t **blob, size_t *bytes);
 void oracle_free(void *p);
 
 /* decode tiles [t_lo, t_hi) into out (M*K elements of the container) and,

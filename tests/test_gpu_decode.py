@@ -83,9 +83,55 @@ def test_c4b_lossless_8192_specials(ep):
     _check(ep, oracle.encode_lossless(w), expect_bits=w)
 
 
+@pytest.mark.parametrize("dtype", ["fp16", "fp8", "fp32"])
+@pytest.mark.parametrize("rows,cols", [(512, 1024), (45, 200), (8192, 1024)])
+def test_lossless_other_dtypes(ep, dtype, rows, cols):
+    npt = oracle.LOSSLESS_DTYPES[dtype][1]
+    rng = np.random.default_rng(rows + cols)
+    if dtype == "fp8":
+        w = rng.integers(0, 256, size=(rows, cols), dtype=np.uint16).astype(np.uint8)
+    else:
+        # realistic exponents plus special values, so the coded byte is skewed
+        f = rng.standard_normal((rows, cols)).astype(np.float32) * 0.02
+        w = f.view(np.uint32) if dtype == "fp32" else f.astype(np.float16).view(np.uint16)
+        w[0, :4] = [0, np.iinfo(npt).max, 1, 0]
+    blob = oracle.encode_lossless(w, dtype)
+    y_o, _ = oracle.decode(blob)
+    db = ep.DeviceBlob(blob)
+    y_g, rs, sym = ep.decode(db, symbols=True)
+    assert rs is None
+    as_bits = {"fp16": torch.int16, "fp8": torch.uint8, "fp32": torch.int32}[dtype]
+    assert (y_g.view(as_bits).cpu().numpy().view(npt) == w).all() and (y_o == w).all()
+    assert (sym.cpu().numpy() == oracle.decode_symbols(blob)).all()
+    y2, _ = ep.decode(db)  # the production path (no symbol dump)
+    assert (y2.view(as_bits).cpu().numpy().view(npt) == w).all()
+
+
+def test_lossless_other_dtypes_batched(ep):
+    rng = np.random.default_rng(3)
+    ws = [rng.standard_normal((r, c)).astype(np.float32).view(np.uint32) for r, c in [(256, 512), (45, 200), (96, 384)]]
+    blobs = [oracle.encode_lossless(w, "fp32") for w in ws]
+    dbs = [ep.DeviceBlob(b) for b in blobs]
+    outs = [d.alloc_out() for d in dbs]
+    ep.BatchDecoder(dbs, outs, ring=0)()
+    for w, o in zip(ws, outs):
+        assert (o.view(torch.int32).cpu().numpy().view(np.uint32) == w).all()
+
+
 def test_lossless_every_bf16_pattern(ep):
     w = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(512, 128)
     _check(ep, oracle.encode_lossless(w), expect_bits=w)
+
+
+def test_large_matrix_two_lanes_per_thread(ep):
+    # 16384 x 10240 = 40960 tiles = 5120 groups of 8: more than one wave of
+    # warps, so the single-stream decode runs two lanes per thread (odd job
+    # counts and ragged tails included in the grid's last CTAs)
+    w = synth.student_t5_bf16(77, 16384, 10240)
+    blob = oracle.encode(w, 4.0)
+    db = ep.DeviceBlob(blob)
+    y, _ = ep.decode(db)
+    assert (_np(y) == oracle.decode_threaded(blob)[0]).all()
 
 
 @pytest.mark.parametrize("rows,cols", [(32, 128), (96, 384), (224, 640), (32, 128 * 13)])
@@ -94,6 +140,26 @@ def test_ragged_and_single_tiles(ep, rows, cols):
     w = synth.student_t5_bf16(rows + cols, rows, cols)
     _check(ep, oracle.encode(w, 4.0))
     _check(ep, oracle.encode(w, 3.0, "fp8"))
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 8), (45, 200), (33, 136), (100, 1000), (31, 120), (257, 3848)])
+def test_general_shapes(ep, rows, cols):
+    # tiles cover the matrix padded to 32 x 128 multiples; the GPU writes only
+    # the true rows x cols values (row stride cols), bit for bit as the oracle
+    w = synth.student_t5_bf16(rows * 3 + cols, rows, cols)
+    for container in ("bf16", "fp16", "fp8", "int8"):
+        _check(ep, oracle.encode(w, 4.0, container))
+    _check(ep, oracle.encode_lossless(w), expect_bits=w)
+
+
+def test_general_shapes_batched(ep):
+    ws = [synth.student_t5_bf16(500 + i, r, c) for i, (r, c) in enumerate([(45, 200), (100, 1000), (1, 8), (33, 136)])]
+    blobs = [oracle.encode(w, 4.0) for w in ws]
+    dbs = [ep.DeviceBlob(b) for b in blobs]
+    outs = [torch.full(d.shape, 5.0, dtype=torch.bfloat16, device="cuda") for d in dbs]
+    ep.BatchDecoder(dbs, outs, ring=0)()
+    for b, o in zip(blobs, outs):
+        assert (_np(o) == oracle.decode(b)[0]).all()
 
 
 def test_zero_and_constant_tensors(ep):

@@ -77,6 +77,16 @@ def test_compressed_linear_small(ep):
     _check(y, x, w_hat)
 
 
+@pytest.mark.parametrize("T,N,K", [(77, 1000, 1000), (5, 48, 200), (300, 264, 136)])
+def test_compressed_linear_general_shapes(ep, T, N, K):
+    w = synth.student_t5_bf16(N + K, N, K)
+    x = synth.normal_bf16(T + K, T, K, std=1.0)
+    blob = oracle.encode(w, 4.0)
+    y = ep.compressed_linear(ep.DeviceBlob(blob), _bf16_dev(x))
+    assert y.shape == (T, N)
+    _check(y, x, oracle.container_to_f64(oracle.decode(blob)[0], "bf16"))
+
+
 def test_compressed_linear_full_size_sampled(ep):
     # X 8192 x 3840 N(0,1), W 10240 x 3840 Student-t at 4 bpp
     w = synth.student_t5_bf16(5, 10240, 3840)

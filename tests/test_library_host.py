@@ -46,6 +46,10 @@ CASES = [
     ("c4_1024x2048_int8_3bpp", lambda: synth.normal_bf16(4, 1024, 2048), 3.0, "int8"),
     ("escape_heavy_6bpp", lambda: synth.rows_outliers_bf16(9, 64, 512, frac=0.05, k_sigma=40.0), 6.0, "bf16"),
     ("tiny_rows_and_zero_rows", lambda: _tiny_rows(), 3.5, "int8"),
+    ("ragged_45x200", lambda: synth.student_t5_bf16(30, 45, 200), 4.0, "bf16"),
+    ("ragged_1x8", lambda: synth.normal_bf16(31, 1, 8), 4.0, "bf16"),
+    ("ragged_100x1000_fp8", lambda: synth.normal_bf16(32, 100, 1000), 3.0, "fp8"),
+    ("ragged_33x136_int8", lambda: synth.rows_outliers_bf16(33, 33, 136), 3.5, "int8"),
 ]
 
 
@@ -87,6 +91,20 @@ def test_lossless_byte_identical_and_exhaustive():
     assert ep.encode(every, lossless=True) == oracle.encode_lossless(every)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp8", "fp32"])
+@pytest.mark.parametrize("shape", [(64, 256), (45, 200), (1, 8), (100, 1000)])
+def test_lossless_dtypes_byte_identical(dtype, shape):
+    ep = _ep()
+    npt = oracle.LOSSLESS_DTYPES[dtype][1]
+    rng = np.random.default_rng(shape[0] * 1000 + shape[1])
+    w = rng.integers(0, np.iinfo(npt).max, size=shape, dtype=npt, endpoint=True)
+    blob = ep.encode(w, container=dtype, lossless=True)
+    assert blob == oracle.encode_lossless(w, dtype)
+    q = ep.query(blob)
+    assert q["mode"] == 1 and q["container"] == oracle.LOSSLESS_DTYPES[dtype][0]
+    assert q["out_elem_bytes"] == np.dtype(npt).itemsize
+
+
 def test_errors():
     ep = _ep()
     w = synth.normal_bf16(5, 64, 256)
@@ -96,8 +114,12 @@ def test_errors():
         ep.encode(bad)
     assert e.value.status == "EP_ERR_NONFINITE"
     with pytest.raises(ep.EntroPackError) as e:
-        ep.encode(w[:, :200].copy())
+        ep.encode(w[:, :204].copy())  # in_features not a multiple of 8
     assert e.value.status == "EP_ERR_SHAPE"
+    with pytest.raises(ep.EntroPackError) as e:
+        ep.encode(w[:0].copy())
+    assert e.value.status == "EP_ERR_SHAPE"
+    assert ep.query(ep.encode(w[:, :200].copy()))["cols"] == 200  # any multiple of 8 is accepted
     with pytest.raises(ep.EntroPackError) as e:
         ep.encode(w, target_bpp=-1.0)
     assert e.value.status == "EP_ERR_INVALID_ARG"

@@ -7,7 +7,10 @@
   rel-L2 ~ sqrt(2 pi e G(E8)) 2^-R and est(Delta) ~ h(N(0,1)) - log2 Delta;
 * actual_bpp >= empirical entropy of the coded symbols + metadata, and
   actual_bpp > target_bpp (the pages report actual above target);
-* rate search lands within one grid step of the target.
+* rate search lands within one grid step of the target;
+* any shape with in_features % 8 == 0: the stream codes the matrix padded
+  to whole tiles, the row steps come from the true columns (RMS computed
+  here with numpy), and decoding returns exactly the true rows x columns.
 """
 import math
 
@@ -28,6 +31,11 @@ def _w(seed=1, M=256, K=1024, std=0.02):
 def _row_steps(blob):
     h = oracle.header(blob)
     return np.frombuffer(blob, dtype=np.float32, count=h["M"], offset=h["rowmeta_off"]).astype(np.float64)
+
+
+def _rn7(v):
+    m, e = np.frexp(v)
+    return np.ldexp(np.rint(m * 128.0), e - 7)
 
 
 @pytest.mark.parametrize("target", [2.5, 4.0])
@@ -168,7 +176,10 @@ def test_rejects_bad_inputs():
         oracle.encode(bad)
     assert e.value.name == "nonfinite"
     with pytest.raises(oracle.OracleError) as e:
-        oracle.encode(w[:48])
+        oracle.encode(np.ascontiguousarray(w[:, :252]))  # in_features not a multiple of 8
+    assert e.value.name == "shape"
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.encode_lossless(np.ascontiguousarray(w[:, :100]))
     assert e.value.name == "shape"
 
 
@@ -184,3 +195,45 @@ def test_corrupt_blob_is_reported():
         assert e.value.name == "corrupt"
     with pytest.raises(oracle.OracleError):
         oracle.decode(bytes(blob[:-16]))
+
+
+@pytest.mark.parametrize("M,K", [(1, 8), (45, 200), (33, 136), (100, 1000), (31, 120)])
+def test_general_shapes(M, K):
+    w = synth.student_t5_bf16(M * 7 + K, M, K)
+    blob = oracle.encode(w, 4.0)
+    h = oracle.header(blob)
+    Mp, Kp = -(-M // 32) * 32, -(-K // 128) * 128
+    assert (h["M"], h["K"], h["n_tiles"]) == (M, K, (Mp // 32) * (Kp // 128))
+    # row steps: RN7 of the RMS over the true columns times Delta_j (numpy, fp64)
+    W = synth.bf16_to_f32(w).astype(np.float64)
+    s = np.sqrt((W * W).sum(axis=1) / K)
+    want = np.where(s > 0, np.clip(_rn7(s * oracle.delta(h["j"])), 2.0 ** -120, 2.0 ** 120), 0.0)
+    assert (_row_steps(blob) == want.astype(np.float32).astype(np.float64)).all()
+    # every true block decodes to the nearest E8 point of w / g; the output is M x K
+    k = oracle.decode_lattice(blob)
+    assert k.shape == (M, K)
+    g = _row_steps(blob)
+    for r in range(M):
+        for c0 in range(0, K, 8):
+            a, c = oracle.e8_nearest(W[r, c0:c0 + 8] / g[r]) if g[r] else (np.zeros(8, np.int64), 0)
+            assert (k[r, c0:c0 + 8] == 2 * a + c).all(), (r, c0)
+    y, _ = oracle.decode(blob)
+    assert y.shape == (M, K)
+    # lossless: bitwise identity on the true region
+    wl = w.copy()
+    wl[0, :8] = [0x0000, 0x8000, 0x7F80, 0xFF80, 0x7FC1, 0x0001, 0x3F80, 0xBF80]
+    yl, _ = oracle.decode(oracle.encode_lossless(wl))
+    assert yl.shape == (M, K) and (yl == wl).all()
+
+
+def test_cropping_rows_keeps_each_rows_code():
+    # rows are normalised one by one, so cropping a matrix to fewer rows (which
+    # pads them back to the same tiles) changes no surviving row's lattice
+    # points at the same resolution index
+    w = synth.normal_bf16(21, 64, 256)
+    b1 = oracle.encode(w, 4.0)
+    b2 = oracle.encode(np.ascontiguousarray(w[:60]), 4.0)
+    h1, h2 = oracle.header(b1), oracle.header(b2)
+    assert (h2["M"], h2["n_tiles"]) == (60, h1["n_tiles"])
+    if h1["j"] == h2["j"]:
+        assert (oracle.decode_lattice(b1)[:60] == oracle.decode_lattice(b2)).all()
