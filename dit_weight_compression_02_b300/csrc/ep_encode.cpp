@@ -10,8 +10,8 @@
 //      coset, the parity-reduced last coordinate given the coset;
 //   5. 12-bit frequency tables over the whole tensor;
 //   6. rANS in independently decodable 32 x 128 tiles, 4 interleaved lanes.
-// Every floating-point step follows the exact operation order written down in
-// FORMAT.md, so that the bytes equal those of any other conforming encoder;
+// Every floating-point step follows the exact operation order that stream
+// format version 1 fixes, so that the bytes equal those of any other conforming encoder;
 // the sources are compiled with -ffp-contract=off.
 #include <algorithm>
 #include <atomic>
@@ -572,7 +572,7 @@ class LossyEncoder {
 };
 
 // --------------------------------------------------------- lossless encode
-// Element split (FORMAT.md §5): the coded byte and the raw bytes of one element.
+// Element split: the coded byte and the raw bytes of one element.
 struct LosslessSplit {
     int container, eb, rb;  // element type, element bytes, raw bytes per element
     uint8_t code(const uint8_t* x, uint8_t* raw) const {

@@ -28,7 +28,7 @@ constexpr double kPeakBound = 15000.0;
 constexpr int kTileHeaderBytes = 24;   // 4 x u32 state + 4 x u16 word counts
 constexpr int kRawBytesPerTile = 4096;  // lossless BF16/FP16: one sign+mantissa byte per element
 
-// Lossless element split (FORMAT.md §5): raw bytes per element kept uncoded
+// Lossless element split: raw bytes per element kept uncoded
 // (BF16/FP16: 1, FP8: 0, FP32: 3) and element sizes in bytes.
 inline int lossless_raw_per_elem(int container) {
     return container == EP_C_FP8_E4M3 ? 0 : (container == EP_C_FP32 ? 3 : 1);

@@ -3,7 +3,7 @@
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
 reference leg may import this package.  It shares no code with the CUDA
 library: its C source (``entropack_oracle.c``) is compiled separately with gcc
-and follows the stream format fixed in FORMAT.md step by step.
+and follows stream format version 1 step by step.
 
 Method: "EntroPack: Fast and Accurate Entropy-Coded Weight Compression at
 Arbitrary Bitrates", Abstract (row-normalised E8 lattice quantisation, a
@@ -102,6 +102,14 @@ def lib():
         L.oracle_decode_lattice.restype = i32
         L.oracle_decode_lattice.argtypes = [P, sz, P, i64, i64]
         L.oracle_convert_f32.argtypes = [i32, i64, P, P]
+        L.oracle_nf4_levels.argtypes = [P]
+        L.oracle_int4_levels.argtypes = [P]
+        L.oracle_q4_roundtrip.restype = f64
+        L.oracle_q4_roundtrip.argtypes = [P, i64, i64, P, P, P, P]
+        L.oracle_e4m3_to_f64.restype = f64
+        L.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        L.oracle_fp8_row_roundtrip.restype = f64
+        L.oracle_fp8_row_roundtrip.argtypes = [P, i64, i64, P]
         _lib = L
     return _lib
 
@@ -248,7 +256,7 @@ def encode_lossless(w_bits: np.ndarray, dtype: str = "bf16") -> bytes:
 
 
 def header(blob: bytes) -> dict:
-    """Header fields (FORMAT.md §6), read with numpy (no codec arithmetic)."""
+    """Header fields of a stream, read with numpy (no codec arithmetic)."""
     h = np.frombuffer(blob[:128], dtype=np.uint8)
     u64 = lambda o: int(h[o:o + 8].view(np.uint64)[0])
     return {
@@ -361,3 +369,42 @@ def container_to_f64(y: np.ndarray, container: str | int, row_scale=None) -> np.
     if row_scale is not None:
         v = v * row_scale.astype(np.float64)[:, None]
     return v
+
+
+def q4_levels(kind: str) -> np.ndarray:
+    """The 16 fp64 levels of a 4-bit comparator codebook: "nf4" (ascending) or "int4" (k/7, then 0)."""
+    cb = np.zeros(16, dtype=np.float64)
+    {"nf4": lib().oracle_nf4_levels, "int4": lib().oracle_int4_levels}[kind](_p(cb))
+    return cb
+
+
+def q4_roundtrip(w_bits: np.ndarray, kind: str = "nf4", block: int = 64):
+    """Block-absmax 4-bit comparator of a BF16 matrix.
+
+    Returns (codes uint8 0..15, FP32 block scales, BF16 reconstruction bits, bits per weight)."""
+    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    n = w_bits.size
+    codes = np.zeros(w_bits.shape, dtype=np.uint8)
+    scales = np.zeros((n + block - 1) // block, dtype=np.float32)
+    recon = np.zeros(w_bits.shape, dtype=np.uint16)
+    levels = q4_levels(kind)
+    bits = lib().oracle_q4_roundtrip(_p(w_bits), n, block, _p(levels), _p(codes), _p(scales), _p(recon))
+    return codes, scales, recon, bits
+
+
+def e4m3_to_f64(b: int) -> float:
+    return lib().oracle_e4m3_to_f64(int(b))
+
+
+def fp8_row_roundtrip(w_bits: np.ndarray):
+    """Per-row-scaled FP8 E4M3 comparator: (BF16 reconstruction bits, bits per weight)."""
+    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    recon = np.zeros(w_bits.shape, dtype=np.uint16)
+    bits = lib().oracle_fp8_row_roundtrip(_p(w_bits), w_bits.shape[0], w_bits.shape[1], _p(recon))
+    return recon, bits
+
+
+def rel_l2(w_hat: np.ndarray, w: np.ndarray) -> float:
+    """Relative L2 weight error ||w_hat - w|| / ||w|| in fp64."""
+    w = np.asarray(w, dtype=np.float64)
+    return float(np.linalg.norm(np.asarray(w_hat, dtype=np.float64) - w) / np.linalg.norm(w))

@@ -73,7 +73,7 @@ static uint16_t get_u16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)
 static uint32_t get_u32(const uint8_t *p) { uint32_t v = 0; for (int i = 3; i >= 0; i--) v = (v << 8) | p[i]; return v; }
 static uint64_t get_u64(const uint8_t *p) { uint64_t v = 0; for (int i = 7; i >= 0; i--) v = (v << 8) | p[i]; return v; }
 static uint64_t align16(uint64_t v) { return (v + 15u) & ~(uint64_t)15u; }
-/* tile-grid dimensions: the matrix is padded with zeros to whole tiles (FORMAT §1) */
+/* tile-grid dimensions: the matrix is padded with zeros to whole tiles */
 static int64_t pad_rows(int64_t M) { return (M + TILE_R - 1) / TILE_R * TILE_R; }
 static int64_t pad_cols(int64_t K) { return (K + TILE_C - 1) / TILE_C * TILE_C; }
 
@@ -92,7 +92,7 @@ double oracle_bf16_to_f64(uint16_t b) {
     return (double)f;
 }
 
-/* block b of a tile -> (row in tile, first column in tile); FORMAT §1 */
+/* block b of a tile -> (row in tile, first column in tile) */
 static void block_place(int b, int *row, int *col) {
     int slab = b / 64, rem = b % 64;
     *row = rem / 2;
@@ -1040,3 +1040,112 @@ void oracle_gemm_f64(const double *x, const double *w, double *y, int64_t T, int
         }
 }
 
+/* ---------------------------------------- fixed-width 4-bit comparators
+   The comparators of the evaluation ("EntroPack: Fast and Accurate
+   Entropy-Coded Weight Compression at Arbitrary Bitrates", Abstract: lower
+   relative L2 weight error than NF4 at a 4-bit target, with less storage;
+   lower errors than fixed-width formats at comparable storage).
+
+   Both are block-absmax 4-bit codebook quantisers: a block of `block`
+   consecutive weights stores its absolute maximum s as FP32 and one 4-bit
+   code per weight (4 + 32 / block bits per weight).  The code of w is the
+   nearest codebook level to w / s, both computed in FP32 (ties to the lower
+   code); the reconstruction is BF16(level * s), one FP32 product rounded to
+   nearest even.
+
+   NF4 codebook (4-bit NormalFloat): quantiles of N(0, 1), scaled so that the
+   extremes are +-1, with an exact zero; 8 non-negative levels at
+   probabilities evenly spaced from 1/2 to 1 - d, and 7 negative levels at
+   probabilities evenly spaced from 1/2 to 1 - d and mirrored, where
+   d = (1/32 + 1/30) / 2 keeps the outermost quantile finite.
+   INT4 codebook (symmetric absmax integer): the 15 levels k / 7, k = -7..7,
+   and a 16th code equal to level 0 (never chosen: ties go to the lower code). */
+static double normal_cdf(double x) { return 0.5 * erfc(-x / sqrt(2.0)); }
+
+static double normal_quantile(double p) { /* bisection on the CDF to the last bit */
+    double lo = -40.0, hi = 40.0;
+    for (int i = 0; i < 200; i++) {
+        double mid = 0.5 * (lo + hi);
+        if (normal_cdf(mid) < p) lo = mid; else hi = mid;
+    }
+    return 0.5 * (lo + hi);
+}
+
+void oracle_nf4_levels(double cb[16]) {
+    const double d = 0.5 * (1.0 / 32.0 + 1.0 / 30.0), top = 1.0 - d;
+    double v[16];
+    int n = 0;
+    for (int i = 0; i < 7; i++) /* negative: 7 probabilities from 1 - d towards 1/2, step (1/2 - d) / 7 */
+        v[n++] = -normal_quantile(top - (0.5 - d) * (double)i / 7.0);
+    v[n++] = 0.0;
+    for (int i = 0; i < 8; i++) /* positive: 8 probabilities from 1 - d towards 1/2, step (1/2 - d) / 8 */
+        v[n++] = normal_quantile(top - (0.5 - d) * (double)i / 8.0);
+    const double mx = normal_quantile(top);
+    for (int i = 0; i < 16; i++) v[i] /= mx;
+    for (int i = 1; i < 16; i++) /* ascending */
+        for (int j = i; j > 0 && v[j] < v[j - 1]; j--) { double t = v[j]; v[j] = v[j - 1]; v[j - 1] = t; }
+    for (int i = 0; i < 16; i++) cb[i] = v[i];
+}
+
+void oracle_int4_levels(double cb[16]) {
+    for (int k = -7; k <= 7; k++) cb[k + 7] = (double)k / 7.0;
+    cb[15] = 0.0;
+}
+
+/* quantise n BF16 weights with a 16-level codebook (FP32 copies of the levels
+   are what the decisions and reconstructions use); codes[i] in 0..15,
+   scales[n / block rounded up], recon[i] BF16 bits.  Returns bits per weight. */
+double oracle_q4_roundtrip(const uint16_t *w, int64_t n, int64_t block, const double levels[16],
+                           uint8_t *codes, float *scales, uint16_t *recon) {
+    float cb[16];
+    for (int k = 0; k < 16; k++) cb[k] = (float)levels[k];
+    for (int64_t b0 = 0, bi = 0; b0 < n; b0 += block, bi++) {
+        const int64_t b1 = b0 + block < n ? b0 + block : n;
+        float s = 0.0f;
+        for (int64_t i = b0; i < b1; i++) {
+            float a = fabsf((float)oracle_bf16_to_f64(w[i]));
+            if (a > s) s = a;
+        }
+        scales[bi] = s;
+        for (int64_t i = b0; i < b1; i++) {
+            const float x = s > 0.0f ? (float)oracle_bf16_to_f64(w[i]) / s : 0.0f;
+            int best = 0;
+            float bd = fabsf(x - cb[0]);
+            for (int k = 1; k < 16; k++) {
+                const float dk = fabsf(x - cb[k]);
+                if (dk < bd) { bd = dk; best = k; }
+            }
+            codes[i] = (uint8_t)best;
+            recon[i] = oracle_f32_to_bf16(cb[best] * s);
+        }
+    }
+    return 4.0 + 32.0 / (double)block;
+}
+
+/* E4M3 value of a byte: bias 7, 3 mantissa bits, subnormals at exponent 0,
+   S.1111.111 is NaN (never produced by the satfinite conversion) */
+double oracle_e4m3_to_f64(uint8_t b) {
+    const int e = (b >> 3) & 0xF, m = b & 7;
+    double v = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    if (e == 15 && m == 7) v = NAN;
+    return (b & 0x80) ? -v : v;
+}
+
+/* FP8 comparator: per-row scale t = max|w| / 448 (FP32), w / t rounded to E4M3
+   (satfinite), reconstruction BF16(e4m3 * t).  8 + 32 / K bits per weight. */
+double oracle_fp8_row_roundtrip(const uint16_t *w, int64_t M, int64_t K, uint16_t *recon) {
+    for (int64_t r = 0; r < M; r++) {
+        float s = 0.0f;
+        for (int64_t c = 0; c < K; c++) {
+            float a = fabsf((float)oracle_bf16_to_f64(w[r * K + c]));
+            if (a > s) s = a;
+        }
+        const float t = s / 448.0f;
+        for (int64_t c = 0; c < K; c++) {
+            const float x = t > 0.0f ? (float)oracle_bf16_to_f64(w[r * K + c]) / t : 0.0f;
+            const uint8_t q = oracle_f32_to_e4m3_satfinite(x);
+            recon[r * K + c] = oracle_f32_to_bf16((float)oracle_e4m3_to_f64(q) * t);
+        }
+    }
+    return 8.0 + 32.0 / (double)K;
+}

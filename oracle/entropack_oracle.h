@@ -12,13 +12,18 @@
  *   fused decode + reconstruction into BF16/FP16/FP8/INT8 -> oracle_decode
  * Lossless tiled ANS ("EntroPack PyTorch Guide", section "Choose a
  * compression contract", TileANSConfig) -> oracle_encode_lossless.
- * The stream layout and every constant are the readings written down in
- * FORMAT.md of this repository.
+ * Comparators of the evaluation (Abstract: lower relative L2 weight error
+ * than NF4 at a 4-bit target, with less storage, and than fixed-width formats
+ * at comparable storage) -> oracle_q4_roundtrip with oracle_nf4_levels /
+ * oracle_int4_levels, oracle_fp8_row_roundtrip.
+ * The stream layout and every constant are this repository's readings of
+ * those passages (stream format version 1).
  *
  * Parity pins (tests/test_oracle_*.py): brute-force E8 search, the E8
  * second moment 929/12960, rANS round trip and code-length bounds,
  * conversions against torch, the Gaussian rate-distortion closed form,
- * bitwise lossless recovery.  Parity unpinned: the exact resolution index
+ * bitwise lossless recovery, NF4 levels through the normal CDF, brute-force
+ * 4-bit quantisation, E4M3 decoding against torch.  Parity unpinned: the exact resolution index
  * chosen by the rate search (only its determinism and its distance to the
  * target are pinned).
  */
@@ -62,7 +67,7 @@ int oracle_select_j(const uint16_t *w, int64_t M, int64_t K, float target_bpp, f
 int oracle_encode(const uint16_t *w, int64_t M, int64_t K, float target_bpp, int container, float sample_frac,
                   uint8_t **blob, size_t *bytes);
 int oracle_encode_lossless(const uint16_t *w, int64_t M, int64_t K, uint8_t **blob, size_t *bytes);
-/* lossless tiled ANS of BF16 (0), FP16 (1), FP8 e4m3 (2) or FP32 (4) elements (FORMAT §5) */
+/* lossless tiled ANS of BF16 (0), FP16 (1), FP8 e4m3 (2) or FP32 (4) elements */
 int oracle_encode_lossless_dtype(const void *w, int64_t M, int64_t K, int dtype, uint8_t **blob, size_t *bytes);
 void oracle_free(void *p);
 
@@ -76,6 +81,16 @@ int oracle_decode_symbols(const uint8_t *blob, size_t bytes, uint8_t *sym_out, i
 int oracle_decode_lattice(const uint8_t *blob, size_t bytes, int32_t *k_out, int64_t t_lo, int64_t t_hi);
 /* batch conversions used by the conversion pins: kind 0 bf16, 1 fp16, 2 e4m3 satfinite, 3 int8 */
 void oracle_convert_f32(int kind, int64_t n, const float *in, void *out);
+
+/* fixed-width comparators: block-absmax 4-bit codebook quantisers (NF4 and
+   INT4 levels; codes, FP32 block scales and BF16 reconstructions; returns the
+   bits per weight) and a per-row-scaled FP8 E4M3 round trip */
+void oracle_nf4_levels(double cb[16]);
+void oracle_int4_levels(double cb[16]);
+double oracle_q4_roundtrip(const uint16_t *w, int64_t n, int64_t block, const double levels[16],
+                           uint8_t *codes, float *scales, uint16_t *recon);
+double oracle_e4m3_to_f64(uint8_t b);
+double oracle_fp8_row_roundtrip(const uint16_t *w, int64_t M, int64_t K, uint16_t *recon);
 
 /* fp64 reference GEMM: y[t, n] = sum_k x[t, k] * w[n, k] for rows t of x */
 void oracle_gemm_f64(const double *x, const double *w, double *y, int64_t T, int64_t N, int64_t K);

@@ -1,4 +1,4 @@
-"""Pins of the oracle's whole lossy codec (FORMAT.md §4).
+"""Pins of the oracle's whole lossy codec.
 
 * every decoded lattice point equals the plain nearest-E8 quantisation of
   w / g_r done here block by block (checks symbols, contexts, escapes,

@@ -1,4 +1,4 @@
-"""Pins of the oracle's container conversions (FORMAT.md §4.5).
+"""Pins of the oracle's container conversions.
 
 The oracle rounds from the format definitions (nearest multiple of the
 quantum of the binade, ties to even); these tests check it against torch's

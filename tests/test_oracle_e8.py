@@ -1,4 +1,4 @@
-"""Pins of the oracle's nearest-E8-point search (FORMAT.md §4.2).
+"""Pins of the oracle's nearest-E8-point search.
 
 E8 = D8 u (D8 + 1/2): the decoder must return a lattice point at minimum
 distance.  Pinned against (1) brute-force enumeration of every candidate

@@ -1,4 +1,4 @@
-"""Pins of the oracle's lossless tiled-ANS path (FORMAT.md §5).
+"""Pins of the oracle's lossless tiled-ANS path.
 
 Recovery must be bitwise ("EntroPack PyTorch Guide", "Start with a tensor
 round trip": numeric closeness is not bitwise equality; include zeros,
@@ -44,7 +44,7 @@ def test_lossless_rate():
     assert 8 + h <= bpp <= 8 + h + 0.15
 
 
-# ------------------------------------------------ other element types (FORMAT §5)
+# ------------------------------------------------ other element types
 def test_all_fp16_patterns_bitwise():
     w = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(512, 128)
     y, _ = oracle.decode(oracle.encode_lossless(w, "fp16"))

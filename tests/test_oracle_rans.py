@@ -1,4 +1,4 @@
-"""Pins of the oracle's rANS coder and 12-bit normaliser (FORMAT.md §2, §3).
+"""Pins of the oracle's rANS coder and 12-bit normaliser.
 
 Independent of the oracle itself: hand-computed golden streams, hand-worked
 normaliser tables, and the information-theoretic code-length bounds of rANS
