@@ -19,6 +19,7 @@ the target).
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 
@@ -89,6 +90,9 @@ def lib():
         L.oracle_select_j.argtypes = [P, i64, i64, f32, f32, P]
         L.oracle_encode.restype = i32
         L.oracle_encode.argtypes = [P, i64, i64, f32, i32, f32, P, P]
+        L.oracle_encode_at.argtypes = [P, i64, i64, f32, i32, i32, f32, P, P]
+        L.oracle_smallest_valid_j.restype = i32
+        L.oracle_smallest_valid_j.argtypes = [P, i64, i64]
         L.oracle_encode_lossless.restype = i32
         L.oracle_encode_lossless.argtypes = [P, i64, i64, P, P]
         L.oracle_encode_lossless_dtype.restype = i32
@@ -237,6 +241,97 @@ def encode(w_bits: np.ndarray, target_bpp: float = 4.0, container: str = "bf16",
     if rc:
         raise OracleError(rc, "encode")
     return _take_blob(ptr, size)
+
+
+def encode_at(w_bits: np.ndarray, j: int, target_bpp: float = 4.0, container: str = "bf16",
+              sample_frac: float = 0.05) -> bytes:
+    """Lossy E8 encode at resolution index j (no rate search); target_bpp is only recorded."""
+    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    ptr = ctypes.c_void_p(0)
+    size = ctypes.c_size_t(0)
+    rc = lib().oracle_encode_at(_p(w_bits), w_bits.shape[0], w_bits.shape[1], target_bpp, int(j),
+                                CONTAINERS[container], sample_frac, ctypes.byref(ptr), ctypes.byref(size))
+    if rc:
+        raise OracleError(rc, "encode_at")
+    return _take_blob(ptr, size)
+
+
+def smallest_valid_j(w_bits: np.ndarray) -> int:
+    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    return lib().oracle_smallest_valid_j(_p(w_bits), w_bits.shape[0], w_bits.shape[1])
+
+
+J_MIN, J_MAX = -640, 128
+
+
+def allocate_bits(layers, avg_bpp: float, sensitivities=None, sample_frac: float = 0.05) -> dict:
+    """Per-layer resolution indices for a whole-model storage budget.
+
+    Reading of the pages' per-layer allocation ("EntroPack PyTorch Guide",
+    "Separate reconstruction metrics from application metrics": different
+    bitrates across layers, allocation recorded; the Chinese overview page:
+    give the limited space to the layers whose errors matter more), driven by
+    the sampled storage estimates (Abstract).  Minimising
+    sum_l alpha_l * n_l * D_l subject to sum_l n_l * R_l <= avg_bpp * sum_l n_l,
+    with the high-resolution E8 error D_l ~ G * Delta_l^2 (the same for every
+    row-normalised layer at one Delta), gives equal slopes:
+    alpha_l * Delta_l^2 constant, i.e. j_l = t - 32 * log2(alpha_l) on the
+    Delta_j = 2^(j / 64) grid.  Steps:
+      1. o_l = round(32 * log2(alpha_l)); j_l(t) = clamp(t - o_l, j_min_l, J_MAX)
+         with j_min_l the layer's smallest admissible index;
+      2. E(t) = sum_l n_l * estimate_l(j_l(t)) bits, budget B = avg_bpp * sum_l n_l;
+      3. t = the smallest shared index with E(t) <= B, by bisection between
+         t_lo = min_l(j_min_l + o_l) and t_hi = max_l(J_MAX + o_l) (t_lo if it
+         already fits, t_hi if nothing fits).
+    Returns {"t", "j": [...], "est_bpp": [...], "offsets": [...], "budget_bits", "est_bits"}.
+    """
+    L = len(layers)
+    alphas = [1.0] * L if sensitivities is None else [float(a) for a in sensitivities]
+    if len(alphas) != L or not all(math.isfinite(a) and a > 0 for a in alphas) or not (avg_bpp > 0):
+        raise ValueError("one positive finite sensitivity per layer and a positive budget are required")
+    n = [int(w.shape[0]) * int(w.shape[1]) for w in layers]
+    jmin = [smallest_valid_j(w) for w in layers]
+    off = [int(round_half_away(32.0 * math.log2(a))) for a in alphas]
+    cache = {}
+
+    def est(l, j):
+        if (l, j) not in cache:
+            cache[(l, j)] = estimate_bpp(layers[l], sample_frac, j)
+        return cache[(l, j)]
+
+    def j_of(l, t):
+        return min(max(t - off[l], jmin[l]), J_MAX)
+
+    def total(t):
+        e = 0.0
+        for l in range(L):
+            e += float(n[l]) * est(l, j_of(l, t))
+        return e
+
+    budget = float(np.float32(avg_bpp)) * float(sum(n))
+    t_lo = min(jmin[l] + off[l] for l in range(L))
+    t_hi = max(J_MAX + off[l] for l in range(L))
+    if total(t_lo) <= budget:
+        t = t_lo
+    elif total(t_hi) > budget:
+        t = t_hi
+    else:
+        lo, hi = t_lo, t_hi
+        while hi - lo > 1:
+            mid = lo + (hi - lo) // 2
+            if total(mid) <= budget:
+                hi = mid
+            else:
+                lo = mid
+        t = hi
+    js = [j_of(l, t) for l in range(L)]
+    return {"t": t, "j": js, "est_bpp": [est(l, js[l]) for l in range(L)], "offsets": off,
+            "budget_bits": budget, "est_bits": total(t)}
+
+
+def round_half_away(x: float) -> float:
+    """Round to the nearest integer, halves away from zero (C's lround)."""
+    return math.copysign(math.floor(abs(x) + 0.5), x)
 
 
 LOSSLESS_DTYPES = {"bf16": (0, np.uint16), "fp16": (1, np.uint16), "fp8": (2, np.uint8), "fp32": (4, np.uint32)}

@@ -612,8 +612,36 @@ static void free_tiles(uint8_t **tb, int64_t n) {
 }
 
 /* --------------------------------------------------------- lossy encoder */
+#define J_SELECT (-100000) /* forced_j value that asks for the rate search */
+
+static int encode_lossy(const uint16_t *w, int64_t M, int64_t K, float target_bpp, int forced_j, int container,
+                        float sample_frac, uint8_t **blob, size_t *bytes);
+
 int oracle_encode(const uint16_t *w, int64_t M, int64_t K, float target_bpp, int container, float sample_frac,
                   uint8_t **blob, size_t *bytes) {
+    return encode_lossy(w, M, K, target_bpp, J_SELECT, container, sample_frac, blob, bytes);
+}
+
+int oracle_encode_at(const uint16_t *w, int64_t M, int64_t K, float target_bpp, int j, int container,
+                     float sample_frac, uint8_t **blob, size_t *bytes) {
+    if (j < J_MIN || j > J_MAX) return O_ERR_ARG;
+    return encode_lossy(w, M, K, target_bpp, j, container, sample_frac, blob, bytes);
+}
+
+int oracle_smallest_valid_j(const uint16_t *w, int64_t M, int64_t K) {
+    if (!w || M <= 0 || K <= 0 || K % 8) return J_MAX + 1;
+    int64_t Mp = pad_rows(M), Kp = pad_cols(K);
+    uint16_t *wp = padded_copy(w, M, K, Mp, Kp);
+    rowstats rs;
+    int j = J_MAX + 1;
+    if (wp && row_stats(wp, M, K, Mp, Kp, &rs) == O_OK) j = smallest_valid_j(&rs);
+    if (wp) free_stats(&rs);
+    free(wp);
+    return j;
+}
+
+static int encode_lossy(const uint16_t *w, int64_t M, int64_t K, float target_bpp, int forced_j, int container,
+                        float sample_frac, uint8_t **blob, size_t *bytes) {
     if (!w || !blob || !bytes) return O_ERR_ARG;
     if (M <= 0 || K <= 0 || K % 8) return O_ERR_SHAPE;
     if (container < O_C_BF16 || container > O_C_INT8) return O_ERR_ARG;
@@ -634,7 +662,14 @@ int oracle_encode(const uint16_t *w, int64_t M, int64_t K, float target_bpp, int
     rowstats rs;
     int rc = row_stats(w, M_true, K_true, M, K, &rs);
     if (rc != O_OK) { free_stats(&rs); free(wp); return rc; }
-    int j = select_with_stats(w, &rs, target_bpp, sample_frac, NULL);
+    int j;
+    if (forced_j == J_SELECT) {
+        j = select_with_stats(w, &rs, target_bpp, sample_frac, NULL);
+    } else {
+        /* a resolution chosen by the caller must keep every row's peak in range */
+        if (forced_j < smallest_valid_j(&rs)) { free_stats(&rs); free(wp); return O_ERR_ARG; }
+        j = forced_j;
+    }
 
     int64_t n_blocks = M * (K / 8);
     int32_t *val = (int32_t *)malloc((size_t)(M * K) * sizeof(int32_t)); /* v of every coordinate */

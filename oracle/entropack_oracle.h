@@ -67,6 +67,12 @@ int oracle_select_j(const uint16_t *w, int64_t M, int64_t K, float target_bpp, f
 int oracle_encode(const uint16_t *w, int64_t M, int64_t K, float target_bpp, int container, float sample_frac,
                   uint8_t **blob, size_t *bytes);
 int oracle_encode_lossless(const uint16_t *w, int64_t M, int64_t K, uint8_t **blob, size_t *bytes);
+/* lossy encode at a given resolution index j (no rate search); target_bpp is
+   only recorded in the header.  j below the smallest admissible index -> error */
+int oracle_encode_at(const uint16_t *w, int64_t M, int64_t K, float target_bpp, int j, int container,
+                     float sample_frac, uint8_t **blob, size_t *bytes);
+/* smallest resolution index whose row steps keep every row's peak in range */
+int oracle_smallest_valid_j(const uint16_t *w, int64_t M, int64_t K);
 /* lossless tiled ANS of BF16 (0), FP16 (1), FP8 e4m3 (2) or FP32 (4) elements */
 int oracle_encode_lossless_dtype(const void *w, int64_t M, int64_t K, int dtype, uint8_t **blob, size_t *bytes);
 void oracle_free(void *p);
