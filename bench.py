@@ -259,6 +259,11 @@ def run_ours(args, rank, world, device):
     if not args.no_linear:
         linear = bench_linear(ep, synth, torch, np, device, stream, peaks)
 
+    comparators = allocation = None
+    if not args.no_linear:
+        comparators = bench_comparators(ep, synth, torch, np, device, stream, peaks)
+        allocation = bench_allocation(ep, synth, torch, np, device, stream, args.target_bpp)
+
     # ---------------------------------------------------- CPU oracle baseline
     cpu = None
     if not args.no_cpu:
@@ -296,6 +301,8 @@ def run_ours(args, rank, world, device):
         "gpu_launches": args.steps,
         "clocks": result["clocks"],
         "linear": linear,
+        "comparators": comparators,
+        "allocation": allocation,
         "cpu_baseline": cpu,
         "setup_s": setup_s,
         "wall_s_timed": wall,
@@ -311,9 +318,9 @@ def bench_linear(ep, synth, torch, np, device, stream, peaks):
     L2-resident workspace, then the GEMM), the same GEMM on dense BF16 W
     (ep_linear_bf16), torch.matmul (cuBLAS) on dense W as the library
     comparator, and the decode alone.  The max relative error of the
-    compressed arm is taken against the oracle's fp64 GEMM on sampled rows.
+    compressed arm is taken against an fp64 GEMM (torch, on the host) of the
+    same X and of W as the library decoded it, on sampled token rows.
     """
-    import oracle
     T, N, K = 8192, 10240, 3840
     flops = 2.0 * T * N * K
     w = synth.student_t5_bf16(5, N, K)
@@ -348,8 +355,8 @@ def bench_linear(ep, synth, torch, np, device, stream, peaks):
         t_dec = timeit(lambda: ep.decode_into(db, ws, None, status, stream))
     ep.sync_status(status, stream)
     rows = np.r_[0:4, 4094:4098, 8188:8192]
-    w_hat = oracle.container_to_f64(oracle.decode_threaded(blob)[0], "bf16")
-    y_ref = oracle.gemm_f64(synth.bf16_to_f32(x_bits[rows]).astype(np.float64), w_hat)
+    w_hat = ws.double().cpu()
+    y_ref = (torch.from_numpy(synth.bf16_to_f32(x_bits[rows])).double() @ w_hat.t()).numpy()
     err = float(np.abs(y_cl[rows] - y_ref).max() / np.abs(y_ref).max())
     peak = peaks.get("bf16_tflops")
     return {"shape": "X 8192x3840 (N(0,1)) by W 10240x3840 (Student-t, 4.0 bpp)", "gflop": flops / 1e9,
@@ -359,6 +366,104 @@ def bench_linear(ep, synth, torch, np, device, stream, peaks):
             "dense_tcgen05_tflops": flops / t_dense / 1e12, "dense_cublas_tflops": flops / t_torch / 1e12,
             "decode_ms": t_dec * 1e3, "overhead_pct_vs_dense_tcgen05": 100.0 * (t_cl / t_dense - 1.0),
             "max_rel_err_vs_fp64": err, "err_rows": "12 sampled token rows", "peak_bf16_tflops": peak}
+
+
+def bench_comparators(ep, synth, torch, np, device, stream, peaks, copies: int = 16):
+    """EntroPack against the fixed-width NF4 / INT4 comparators on one FFN layer.
+
+    W is 10240 x 3840 Student-t (nu = 5) BF16.  Relative L2 weight error
+    ||W_hat - W|| / ||W|| (fp64, on the device) of EntroPack at a 4-bit target
+    and of NF4 / INT4 with block 64 and FP32 scales (4.5 bits per weight), all
+    reconstructed by the library's kernels.  The NF4 reconstruction kernel is
+    also timed on `copies` concatenated copies of the layer's codes (inputs
+    and outputs far larger than L2) for its own HBM roofline.
+    """
+    N, K = 10240, 3840
+    n = N * K
+    w = synth.student_t5_bf16(7, N, K)
+    w_dev = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).to(device)
+    w64 = w_dev.double()
+    wnorm = torch.linalg.vector_norm(w64).item()
+
+    def rel(y):
+        return torch.linalg.vector_norm(y.double() - w64).item() / wnorm
+
+    out = {"layer": "W 10240x3840 Student-t nu=5 std 0.02 (BF16)"}
+    blob = ep.encode(w, 4.0)
+    db = ep.DeviceBlob(blob, device=device)
+    y_ep, _ = ep.decode(db, stream=stream)
+    out["entropack_4bpp"] = {"bits_per_weight": 8.0 * len(blob) / n, "rel_l2": rel(y_ep)}
+    for kind in ("nf4", "int4"):
+        q = ep.q4_encode(w, kind, 64)
+        codes = torch.from_numpy(q.codes).to(device)
+        scales = torch.from_numpy(q.scales).to(device)
+        with torch.cuda.stream(stream):
+            y = ep.q4_decode(codes, scales, q.levels, (N, K), 64, stream=stream)
+        torch.cuda.synchronize(device)
+        out[f"{kind}_b64"] = {"bits_per_weight": q.bits_per_weight, "rel_l2": rel(y)}
+        if kind != "nf4":
+            continue
+        big_codes, big_scales = codes.repeat(copies), scales.repeat(copies)
+        big_out = torch.empty(copies * n, dtype=torch.bfloat16, device=device)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                ep.q4_decode(big_codes, big_scales, q.levels, (copies * n,), 64, out=big_out, stream=stream)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 10
+            a.record(stream)
+            for _ in range(reps):
+                ep.q4_decode(big_codes, big_scales, q.levels, (copies * n,), 64, out=big_out, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize(device)
+        t = a.elapsed_time(b) / reps / 1e3
+        alg = copies * n * (0.5 + 4.0 / 64 + 2.0)
+        out["nf4_b64"].update({
+            "decode_gparams_s": copies * n / t / 1e9, "decode_ms": t * 1e3, "decode_params": copies * n,
+            "roofline": {"bound": "hbm", "achieved": alg / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": alg / t / 1e9 / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": alg,
+                         "kernel": "q4_decode_kernel"}})
+        del big_codes, big_scales, big_out
+    out["rel_l2_entropack_over_nf4"] = out["entropack_4bpp"]["rel_l2"] / out["nf4_b64"]["rel_l2"]
+    return out
+
+
+def bench_allocation(ep, synth, torch, np, device, stream, avg_bpp: float = 4.0):
+    """Per-layer bit allocation on one DiT block (7 layers, 177 M params) under one budget.
+
+    Sensitivities: 2 for the attention projections (q, k, v, o), 1 for the
+    FFN (an illustrative choice).  Reported: the host time of
+    ep_allocate_bits, each layer's index and bits, and the sensitivity-
+    weighted squared relative L2 error sum_l alpha_l n_l D_l of the allocated
+    block against every layer encoded at the average target, both decoded
+    by the library's batched kernel and compared on the device.
+    """
+    names = ["q", "k", "v", "o", "up", "gate", "down"]
+    shapes = model_layers(1)
+    sens = [2.0] * 4 + [1.0] * 3
+    ws = [synth.student_t5_bf16(3 + i, r, c) for i, (r, c) in enumerate(shapes)]
+    t0 = time.perf_counter()
+    plan = ep.allocate_bits(ws, avg_bpp, sens)
+    t_alloc = time.perf_counter() - t0
+    arms = {"allocated": [ep.encode(w, e, j=j) for w, j, e in zip(ws, plan["j"], plan["est_bpp"])],
+            "uniform": [ep.encode(w, avg_bpp) for w in ws]}
+    outs = [torch.empty((r, c), dtype=torch.bfloat16, device=device) for r, c in shapes]
+    src = [torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).to(device) for w in ws]
+    res = {"layers": "one DiT block at hidden 3840: q, k, v, o 3840x3840; up, gate 10240x3840; down 3840x10240",
+           "sensitivities": dict(zip(names, sens)), "avg_bpp_budget": avg_bpp, "allocate_host_s": t_alloc,
+           "shared_index": plan["t"], "j": dict(zip(names, plan["j"])),
+           "est_bpp": dict(zip(names, [round(e, 4) for e in plan["est_bpp"]]))}
+    n = [r * c for r, c in shapes]
+    for arm, blobs in arms.items():
+        bd = ep.BatchDecoder([ep.DeviceBlob(b, device=device) for b in blobs], outs)
+        bd(stream)
+        rel = [(torch.linalg.vector_norm(o.double() - s_.double()) / torch.linalg.vector_norm(s_.double())).item()
+               for o, s_ in zip(outs, src)]
+        res[arm] = {"actual_bpp": 8.0 * sum(len(b) for b in blobs) / sum(n),
+                    "rel_l2": dict(zip(names, [round(v, 5) for v in rel])),
+                    "weighted_sq_error": sum(a * nl * r * r for a, nl, r in zip(sens, n, rel)) / sum(n)}
+    res["weighted_error_ratio_allocated_over_uniform"] = (res["allocated"]["weighted_sq_error"]
+                                                          / res["uniform"]["weighted_sq_error"])
+    return res
 
 
 def cpu_baseline(blobs, shapes, n_layers):
@@ -411,7 +516,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--blocks", type=int, default=30)

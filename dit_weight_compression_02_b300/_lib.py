@@ -44,6 +44,10 @@ class EpBatchPlan(ctypes.Structure):
 
 
 # name -> (restype, argtypes); mirrors include/entropack.h
+class EpLayerRef(ctypes.Structure):
+    _fields_ = [("w", P), ("rows", i64), ("cols", i64), ("sensitivity", f32)]
+
+
 SIGNATURES = {
     "ep_version": (i32, []),
     "ep_status_string": (ctypes.c_char_p, [i32]),
@@ -58,8 +62,14 @@ SIGNATURES = {
     "ep_batch_decode": (i32, [ctypes.POINTER(EpBatchPlan), P, P]),
     "ep_sync_status": (i32, [P, P]),
     "ep_batch_decode_static": (i32, [ctypes.POINTER(EpBatchItem), i64, i32, P, P]),
-    "ep_linear_bf16": (i32, [P, P, P, i64, i64, i64, P, P]),
-    "ep_compressed_linear": (i32, [P, P, sz, P, i64, P, i32, P, sz, P, P]),
+    "ep_linear_bf16": (i32, [P, P, P, P, i64, i64, i64, P, P]),
+    "ep_compressed_linear": (i32, [P, P, sz, P, i64, P, P, i32, P, sz, P, P]),
+    "ep_encode_at": (i32, [P, i64, i64, ctypes.POINTER(EpParams), i32, ctypes.POINTER(P), ctypes.POINTER(sz)]),
+    "ep_estimate_bpp": (i32, [P, i64, i64, f32, i32, i32, ctypes.POINTER(f64), ctypes.POINTER(i32)]),
+    "ep_allocate_bits": (i32, [ctypes.POINTER(EpLayerRef), i64, f32, f32, i32, P, P, ctypes.POINTER(i32)]),
+    "ep_q4_levels": (i32, [i32, P]),
+    "ep_q4_encode": (i32, [P, i64, i64, P, P, P, i32]),
+    "ep_q4_decode": (i32, [P, P, i64, i64, P, P, P]),
 }
 
 for _name, (_res, _args) in SIGNATURES.items():

@@ -16,7 +16,7 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from ._lib import EpBatchItem, EpBatchPlan, EpInfo, EpParams, EntroPackError, check, lib
+from ._lib import EpBatchItem, EpBatchPlan, EpInfo, EpLayerRef, EpParams, EntroPackError, check, lib
 
 CONTAINERS = {"bf16": 0, "fp16": 1, "fp8": 2, "int8": 3, "fp32": 4}
 CONTAINER_DTYPES = {0: torch.bfloat16, 1: torch.float16, 2: torch.float8_e4m3fn, 3: torch.int8, 4: torch.float32}
@@ -71,12 +71,14 @@ def element_bits(w, dtype: str) -> np.ndarray:
 
 
 def encode(w_bits: np.ndarray, target_bpp: float = 4.0, container: str = "bf16", lossless: bool = False,
-           sample_frac: float = 0.05, n_threads: int = 0) -> bytes:
+           sample_frac: float = 0.05, n_threads: int = 0, j: int | None = None) -> bytes:
     """ep_encode: a rows x cols matrix -> stream bytes.
 
     Lossy: BF16 bits in, decoded into `container`.  Lossless: elements of the
     type `container` names (bf16, fp16, fp8 or fp32; a torch tensor's own
-    dtype is used when it is one of those), restored bit for bit.
+    dtype is used when it is one of those), restored bit for bit.  With `j`
+    (lossy only) the stream is coded at that resolution index through
+    ep_encode_at, with no rate search.
     """
     if lossless:
         if isinstance(w_bits, torch.Tensor) and w_bits.dtype in _TORCH_TO_LOSSLESS:
@@ -90,12 +92,49 @@ def encode(w_bits: np.ndarray, target_bpp: float = 4.0, container: str = "bf16",
                  float(sample_frac), int(n_threads))
     out = ctypes.c_void_p(0)
     size = ctypes.c_size_t(0)
-    check(lib.ep_encode(_ptr(w_bits), w_bits.shape[0], w_bits.shape[1], ctypes.byref(p), ctypes.byref(out),
-                        ctypes.byref(size)), "ep_encode")
+    if j is not None:
+        if lossless:
+            raise ValueError("a resolution index applies to lossy streams only")
+        check(lib.ep_encode_at(_ptr(w_bits), w_bits.shape[0], w_bits.shape[1], ctypes.byref(p), int(j),
+                               ctypes.byref(out), ctypes.byref(size)), "ep_encode_at")
+    else:
+        check(lib.ep_encode(_ptr(w_bits), w_bits.shape[0], w_bits.shape[1], ctypes.byref(p), ctypes.byref(out),
+                            ctypes.byref(size)), "ep_encode")
     try:
         return ctypes.string_at(out, size.value)
     finally:
         lib.ep_free(out)
+
+
+def estimate_bpp(w_bits, j: int, sample_frac: float = 0.05, n_threads: int = 0):
+    """ep_estimate_bpp: (sampled coded bits per parameter at index j, smallest admissible index)."""
+    w = bf16_bits(w_bits)
+    bpp = ctypes.c_double(0.0)
+    jmin = ctypes.c_int32(0)
+    check(lib.ep_estimate_bpp(_ptr(w), w.shape[0], w.shape[1], float(sample_frac), int(j), int(n_threads),
+                              ctypes.byref(bpp), ctypes.byref(jmin)), "ep_estimate_bpp")
+    return bpp.value, jmin.value
+
+
+def allocate_bits(weights, avg_bpp: float, sensitivities=None, sample_frac: float = 0.05, n_threads: int = 0) -> dict:
+    """ep_allocate_bits: per-layer resolution indices for a model-level storage budget.
+
+    weights: BF16 matrices (tensors or uint16 arrays); sensitivities: one
+    positive weight per layer for its squared relative error (default 1).
+    Returns {"t": shared index, "j": [...], "est_bpp": [...]}.
+    """
+    mats = [bf16_bits(w) for w in weights]
+    n = len(mats)
+    sens = [1.0] * n if sensitivities is None else [float(a) for a in sensitivities]
+    if len(sens) != n:
+        raise ValueError("one sensitivity per layer")
+    refs = (EpLayerRef * n)(*[EpLayerRef(m.ctypes.data, m.shape[0], m.shape[1], a) for m, a in zip(mats, sens)])
+    js = np.zeros(n, dtype=np.int32)
+    est = np.zeros(n, dtype=np.float64)
+    t = ctypes.c_int32(0)
+    check(lib.ep_allocate_bits(refs, n, float(avg_bpp), float(sample_frac), int(n_threads), _ptr(js), _ptr(est),
+                               ctypes.byref(t)), "ep_allocate_bits")
+    return {"t": t.value, "j": [int(v) for v in js], "est_bpp": [float(v) for v in est]}
 
 
 def query(blob) -> dict:
@@ -209,15 +248,23 @@ def _check_bf16_2d(t: torch.Tensor, name: str) -> None:
         raise ValueError(f"{name} must be a contiguous 2-D BF16 CUDA tensor")
 
 
-def linear_bf16(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None, status=None, stream=None):
-    """ep_linear_bf16: Y = X W^T on the tcgen05 GEMM (dense BF16 W)."""
+def _check_bias(bias: torch.Tensor | None, rows: int) -> None:
+    if bias is not None and (bias.dtype != torch.bfloat16 or bias.dim() != 1 or bias.shape[0] != rows
+                             or not bias.is_cuda or not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous 1-D BF16 CUDA tensor of out_features elements")
+
+
+def linear_bf16(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None, status=None, stream=None,
+                bias: torch.Tensor | None = None):
+    """ep_linear_bf16: Y = X W^T (+ bias) on the tcgen05 GEMM (dense BF16 W)."""
     _check_bf16_2d(x, "x")
     _check_bf16_2d(w, "w")
     if x.shape[1] != w.shape[1]:
         raise ValueError("x and w disagree on in_features")
+    _check_bias(bias, w.shape[0])
     y = torch.empty((x.shape[0], w.shape[0]), dtype=torch.bfloat16, device=x.device) if out is None else out
     st = torch.zeros(1, dtype=torch.int32, device=x.device) if status is None else status
-    check(lib.ep_linear_bf16(_ptr(x), _ptr(w), _ptr(y), x.shape[0], w.shape[0], w.shape[1], _ptr(st),
+    check(lib.ep_linear_bf16(_ptr(x), _ptr(w), _ptr(y), _ptr(bias), x.shape[0], w.shape[0], w.shape[1], _ptr(st),
                              _stream_handle(stream)), "ep_linear_bf16")
     if status is None:
         sync_status(st, stream)
@@ -226,22 +273,71 @@ def linear_bf16(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = Non
 
 def compressed_linear(db: DeviceBlob, x: torch.Tensor, mode: int = LINEAR_DECODE_THEN_GEMM,
                       out: torch.Tensor | None = None, workspace: torch.Tensor | None = None, status=None,
-                      stream=None):
-    """ep_compressed_linear: Y = X W^T with W decoded from `db` by the library's kernels."""
+                      stream=None, bias: torch.Tensor | None = None):
+    """ep_compressed_linear: Y = X W^T (+ bias) with W decoded from `db` by the library's kernels."""
     _check_bf16_2d(x, "x")
     rows, cols = db.shape
     if x.shape[1] != cols:
         raise ValueError("x does not match the stream's in_features")
+    _check_bias(bias, rows)
     y = torch.empty((x.shape[0], rows), dtype=torch.bfloat16, device=x.device) if out is None else out
     if mode == LINEAR_DECODE_THEN_GEMM and workspace is None:
         workspace = torch.empty(rows * cols, dtype=torch.bfloat16, device=x.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = torch.zeros(1, dtype=torch.int32, device=x.device) if status is None else status
     check(lib.ep_compressed_linear(_ptr(db.host), _ptr(db.device), db.nbytes, _ptr(x), x.shape[0], _ptr(y),
-                                   int(mode), _ptr(workspace), ws_bytes, _ptr(st), _stream_handle(stream)),
+                                   _ptr(bias), int(mode), _ptr(workspace), ws_bytes, _ptr(st), _stream_handle(stream)),
           "ep_compressed_linear")
     if status is None:
         sync_status(st, stream)
+    return y
+
+
+# ------------------------------------------------- fixed-width comparators
+Q4_KINDS = {"nf4": 0, "int4": 1}
+
+
+def q4_levels(kind: str = "nf4") -> np.ndarray:
+    """ep_q4_levels: the 16 FP32 levels of the NF4 or INT4 comparator codebook."""
+    lv = np.zeros(16, dtype=np.float32)
+    check(lib.ep_q4_levels(Q4_KINDS[kind], _ptr(lv)), "ep_q4_levels")
+    return lv
+
+
+@dataclass
+class Q4Tensor:
+    """A block-absmax 4-bit comparator encoding (host arrays)."""
+    codes: np.ndarray  # uint8, n / 2 (two codes per byte, low nibble first)
+    scales: np.ndarray  # float32, one per block
+    levels: np.ndarray  # float32[16]
+    shape: tuple
+    block: int
+
+    @property
+    def bits_per_weight(self) -> float:
+        n = int(np.prod(self.shape))
+        return 8.0 * (self.codes.nbytes + self.scales.nbytes) / n
+
+
+def q4_encode(w_bits, kind: str = "nf4", block: int = 64, n_threads: int = 0) -> Q4Tensor:
+    """ep_q4_encode: NF4 / INT4 encoding of BF16 weights on the host."""
+    w = bf16_bits(w_bits)
+    n = w.size
+    codes = np.zeros(n // 2 + (n & 1), dtype=np.uint8)
+    scales = np.zeros((n + block - 1) // block, dtype=np.float32)
+    lv = q4_levels(kind)
+    check(lib.ep_q4_encode(_ptr(w), n, block, _ptr(lv), _ptr(codes), _ptr(scales), int(n_threads)), "ep_q4_encode")
+    return Q4Tensor(codes, scales, lv, tuple(w.shape), block)
+
+
+def q4_decode(codes: torch.Tensor, scales: torch.Tensor, levels: np.ndarray, shape, block: int = 64,
+              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """ep_q4_decode: BF16 reconstruction of a comparator encoding on the GPU (device codes / scales)."""
+    n = int(np.prod(shape))
+    y = torch.empty(shape, dtype=torch.bfloat16, device=codes.device) if out is None else out
+    lv = np.ascontiguousarray(levels, dtype=np.float32)
+    check(lib.ep_q4_decode(_ptr(codes), _ptr(scales), n, block, _ptr(lv), _ptr(y), _stream_handle(stream)),
+          "ep_q4_decode")
     return y
 
 
@@ -337,9 +433,8 @@ class CompressedLinear(torch.nn.Module):
             self._status = torch.zeros(1, dtype=torch.int32, device=dev)
         lead = x.shape[:-1]
         x2 = x.reshape(-1, x.shape[-1]).to(torch.bfloat16).contiguous()
-        y = compressed_linear(self.ct.blob, x2, LINEAR_DECODE_THEN_GEMM, workspace=self._ws, status=self._status)
-        if self.bias is not None:
-            y = y + self.bias
+        y = compressed_linear(self.ct.blob, x2, LINEAR_DECODE_THEN_GEMM, workspace=self._ws, status=self._status,
+                              bias=self.bias)  # the bias is added in the GEMM's epilogue
         return y.reshape(*lead, self.out_features)
 
     def check_status(self):
@@ -347,7 +442,35 @@ class CompressedLinear(torch.nn.Module):
             sync_status(self._status)
 
 
+def compress_linears(linears: dict, avg_bpp: float, sensitivities: dict | None = None, sample_frac: float = 0.05,
+                     device="cuda"):
+    """Compress several linear layers under one storage budget (ep_allocate_bits + ep_encode_at).
+
+    linears: name -> torch.nn.Linear; sensitivities: name -> alpha (default 1).
+    Returns (name -> CompressedLinear, record), where the record keeps, per
+    layer, the sensitivity, the resolution index, the estimated and the actual
+    bits per parameter, so the allocation can be reproduced and explained.
+    """
+    names = list(linears)
+    weights = [linears[k].weight.detach().to(torch.bfloat16) for k in names]
+    sens = [float((sensitivities or {}).get(k, 1.0)) for k in names]
+    plan = allocate_bits(weights, avg_bpp, sens, sample_frac)
+    out, record = {}, {"avg_bpp_budget": float(avg_bpp), "shared_index": plan["t"], "layers": {}}
+    for k, w, a, j, e in zip(names, weights, sens, plan["j"], plan["est_bpp"]):
+        blob = encode(bf16_bits(w), e, "bf16", sample_frac=sample_frac, j=j)
+        ct = CompressedTensor(blob, EntroPackLossyConfig(e, "bf16", sample_frac), device=device)
+        lin = linears[k]
+        out[k] = CompressedLinear(ct, None if lin.bias is None else lin.bias.detach().to(device))
+        record["layers"][k] = {"sensitivity": a, "j": j, "est_bpp": e, "actual_bpp": ct.actual_bpp,
+                               "params": int(w.numel())}
+    n_tot = sum(v["params"] for v in record["layers"].values())
+    record["actual_bpp"] = sum(v["actual_bpp"] * v["params"] for v in record["layers"].values()) / n_tot
+    return out, record
+
+
 __all__ = ["encode", "query", "actual_bpp", "DeviceBlob", "decode", "decode_into", "sync_status", "BatchDecoder",
            "linear_bf16", "compressed_linear", "LINEAR_DECODE_THEN_GEMM", "LINEAR_FUSED",
            "EntroPackLossyConfig", "TileANSConfig", "CompressedTensor", "compress", "decompress",
-           "CompressedLinear", "EntroPackError", "CONTAINERS", "CONTAINER_DTYPES"]
+           "CompressedLinear", "EntroPackError", "CONTAINERS", "CONTAINER_DTYPES",
+           "q4_levels", "q4_encode", "q4_decode", "Q4Tensor", "Q4_KINDS",
+           "estimate_bpp", "allocate_bits", "compress_linears"]

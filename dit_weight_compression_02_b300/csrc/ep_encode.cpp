@@ -14,6 +14,9 @@
 // format version 1 fixes, so that the bytes equal those of any other conforming encoder;
 // the sources are compiled with -ffp-contract=off.
 #include <algorithm>
+#include <climits>
+#include <map>
+#include <memory>
 #include <atomic>
 #include <cmath>
 #include <cstdlib>
@@ -331,9 +334,30 @@ class LossyEncoder {
     LossyEncoder(const uint16_t* w, int64_t M, int64_t K, int64_t Mt, int64_t Kt, const ep_params& p, int threads)
         : w_(w), M_(M), K_(K), Mt_(Mt), Kt_(Kt), p_(p), threads_(threads) {}
 
-    ep_status run(uint8_t** blob, size_t* bytes) {
+    static constexpr int kSelectJ = -100000;  // run(): choose j by the rate search
+
+    // pieces of the rate search, used on their own by the model-level allocation
+    void prepare() { row_stats(); }
+    int smallest_admissible() const {
+        int lo = kJMin, hi = kJMax;
+        if (admissible(lo)) return lo;
+        while (hi - lo > 1) {
+            const int mid = lo + (hi - lo) / 2;
+            (admissible(mid) ? hi : lo) = mid;
+        }
+        return hi;
+    }
+    double estimate_at(int j) const { return estimate(j); }
+
+    ep_status run(uint8_t** blob, size_t* bytes, int forced_j = kSelectJ) {
         row_stats();
-        const int j = choose_j();
+        int j;
+        if (forced_j == kSelectJ) {
+            j = choose_j();
+        } else {
+            if (forced_j > kJMax || forced_j < smallest_admissible()) return EP_ERR_INVALID_ARG;
+            j = forced_j;
+        }
         g_.assign((size_t)M_, 0.f);
         for (int64_t r = 0; r < M_; r++) g_[r] = (float)step_of(rows_.rms[r], j);
         ep_status st = quantise_all();
@@ -440,14 +464,7 @@ class LossyEncoder {
     }
 
     int choose_j() const {
-        int lo = kJMin, hi = kJMax;
-        if (!admissible(lo)) {
-            while (hi - lo > 1) {
-                const int mid = lo + (hi - lo) / 2;
-                (admissible(mid) ? hi : lo) = mid;
-            }
-            lo = hi;
-        }
+        int lo = smallest_admissible(), hi = kJMax;
         const double T = (double)p_.target_bpp;
         const int j_lo = lo;
         double e_lo = estimate(j_lo);
@@ -649,8 +666,27 @@ ep_status encode_lossless(const uint8_t* w, int64_t M, int64_t K, int64_t Mt, in
 }  // namespace
 }  // namespace ep
 
-extern "C" ep_status ep_encode(const void* w_in, int64_t rows, int64_t cols, const ep_params* p, uint8_t** blob,
-                               size_t* blob_bytes) {
+namespace {
+
+bool any_nonfinite_bf16(const uint16_t* w, int64_t rows, int64_t cols, int threads) {
+    std::atomic<bool> nonfinite{false};
+    ep::parallel_for(rows, threads, [&](int64_t r0, int64_t r1, int) {
+        for (int64_t i = r0 * cols; i < r1 * cols; i++)
+            if ((w[i] & 0x7F80) == 0x7F80) {
+                nonfinite = true;
+                return;
+            }
+    });
+    return nonfinite;
+}
+
+int thread_count(int32_t requested) {
+    const int t = requested > 0 ? requested : (int)std::max(1u, std::thread::hardware_concurrency());
+    return std::min(t, 256);
+}
+
+ep_status encode_impl(const void* w_in, int64_t rows, int64_t cols, const ep_params* p, int forced_j, uint8_t** blob,
+                      size_t* blob_bytes) {
     const uint16_t* w = static_cast<const uint16_t*>(w_in);  // lossy input: BF16 bit patterns
     if (!w || !p || !blob || !blob_bytes) return EP_ERR_INVALID_ARG;
     *blob = nullptr;
@@ -658,8 +694,7 @@ extern "C" ep_status ep_encode(const void* w_in, int64_t rows, int64_t cols, con
     if (rows <= 0 || cols <= 0 || cols % 8) return EP_ERR_SHAPE;
     if (rows > ((int64_t)1 << 40) || cols > ((int64_t)1 << 40)) return EP_ERR_SHAPE;
     if (p->mode != EP_MODE_LOSSY_E8 && p->mode != EP_MODE_LOSSLESS_TILEANS) return EP_ERR_INVALID_ARG;
-    int threads = p->n_threads > 0 ? p->n_threads : (int)std::max(1u, std::thread::hardware_concurrency());
-    threads = std::min(threads, 256);
+    const int threads = thread_count(p->n_threads);
     try {
         // tiles cover the matrix padded with zeros to whole 32 x 128 tiles
         const int64_t Mp = (rows + ep::kTileRows - 1) / ep::kTileRows * ep::kTileRows;
@@ -682,17 +717,117 @@ extern "C" ep_status ep_encode(const void* w_in, int64_t rows, int64_t cols, con
         if (!(p->target_bpp > 0.f) || !std::isfinite(p->target_bpp)) return EP_ERR_INVALID_ARG;
         ep_params q = *p;
         if (!(q.sample_frac > 0.f) || !std::isfinite(q.sample_frac)) q.sample_frac = 0.05f;
-        std::atomic<bool> nonfinite{false};
-        ep::parallel_for(rows, threads, [&](int64_t r0, int64_t r1, int) {
-            for (int64_t i = r0 * cols; i < r1 * cols; i++)
-                if ((w[i] & 0x7F80) == 0x7F80) {
-                    nonfinite = true;
-                    return;
-                }
-        });
-        if (nonfinite) return EP_ERR_NONFINITE;
+        if (any_nonfinite_bf16(w, rows, cols, threads)) return EP_ERR_NONFINITE;
         ep::LossyEncoder enc(reinterpret_cast<const uint16_t*>(wp), Mp, Kp, rows, cols, q, threads);
-        return enc.run(blob, blob_bytes);
+        return enc.run(blob, blob_bytes, forced_j);
+    } catch (const std::bad_alloc&) {
+        return EP_ERR_NOMEM;
+    }
+}
+
+}  // namespace
+
+extern "C" ep_status ep_encode(const void* w_in, int64_t rows, int64_t cols, const ep_params* p, uint8_t** blob,
+                               size_t* blob_bytes) {
+    return encode_impl(w_in, rows, cols, p, ep::LossyEncoder::kSelectJ, blob, blob_bytes);
+}
+
+extern "C" ep_status ep_encode_at(const void* w, int64_t rows, int64_t cols, const ep_params* p, int32_t j,
+                                  uint8_t** blob, size_t* blob_bytes) {
+    if (!p || p->mode != EP_MODE_LOSSY_E8) return EP_ERR_INVALID_ARG;
+    if (j < ep::kJMin || j > ep::kJMax) return EP_ERR_INVALID_ARG;
+    return encode_impl(w, rows, cols, p, j, blob, blob_bytes);
+}
+
+extern "C" ep_status ep_estimate_bpp(const uint16_t* w, int64_t rows, int64_t cols, float sample_frac, int32_t j,
+                                     int32_t n_threads, double* bpp, int32_t* j_min) {
+    if (!w || !bpp) return EP_ERR_INVALID_ARG;
+    if (rows <= 0 || cols <= 0 || cols % 8 || rows > ((int64_t)1 << 40) || cols > ((int64_t)1 << 40))
+        return EP_ERR_SHAPE;
+    if (j < ep::kJMin || j > ep::kJMax) return EP_ERR_INVALID_ARG;
+    const int threads = thread_count(n_threads);
+    try {
+        if (any_nonfinite_bf16(w, rows, cols, threads)) return EP_ERR_NONFINITE;
+        ep_params q{};
+        q.sample_frac = sample_frac > 0.f && std::isfinite(sample_frac) ? sample_frac : 0.05f;
+        // the rate search reads only true rows and columns: no padding needed
+        ep::LossyEncoder enc(w, rows, cols, rows, cols, q, threads);
+        enc.prepare();
+        *bpp = enc.estimate_at(j);
+        if (j_min) *j_min = enc.smallest_admissible();
+        return EP_OK;
+    } catch (const std::bad_alloc&) {
+        return EP_ERR_NOMEM;
+    }
+}
+
+extern "C" ep_status ep_allocate_bits(const ep_layer_ref* layers, int64_t n_layers, float avg_bpp, float sample_frac,
+                                      int32_t n_threads, int32_t* j_out, double* est_bpp_out, int32_t* t_out) {
+    if (!layers || !j_out || n_layers <= 0) return EP_ERR_INVALID_ARG;
+    if (!(avg_bpp > 0.f) || !std::isfinite(avg_bpp)) return EP_ERR_INVALID_ARG;
+    for (int64_t l = 0; l < n_layers; l++) {
+        const ep_layer_ref& L = layers[l];
+        if (!L.w || !(L.sensitivity > 0.f) || !std::isfinite(L.sensitivity)) return EP_ERR_INVALID_ARG;
+        if (L.rows <= 0 || L.cols <= 0 || L.cols % 8 || L.rows > ((int64_t)1 << 40) || L.cols > ((int64_t)1 << 40))
+            return EP_ERR_SHAPE;
+    }
+    const int threads = thread_count(n_threads);
+    try {
+        ep_params q{};
+        q.sample_frac = sample_frac > 0.f && std::isfinite(sample_frac) ? sample_frac : 0.05f;
+        const size_t nl = (size_t)n_layers;
+        std::vector<std::unique_ptr<ep::LossyEncoder>> enc(nl);
+        std::vector<int> jmin(nl), off(nl);
+        std::vector<std::map<int, double>> memo(nl);
+        double n_total = 0.0;
+        for (size_t l = 0; l < nl; l++) {
+            const ep_layer_ref& L = layers[l];
+            if (any_nonfinite_bf16(L.w, L.rows, L.cols, threads)) return EP_ERR_NONFINITE;
+            enc[l].reset(new ep::LossyEncoder(L.w, L.rows, L.cols, L.rows, L.cols, q, threads));
+            enc[l]->prepare();
+            jmin[l] = enc[l]->smallest_admissible();
+            // equal Lagrangian slopes: alpha * Delta^2 constant, Delta_j = 2^(j / 64)
+            off[l] = (int)std::lround(32.0 * std::log2((double)L.sensitivity));
+            n_total += (double)(L.rows * L.cols);
+        }
+        auto j_of = [&](size_t l, int t) { return std::min(std::max(t - off[l], jmin[l]), ep::kJMax); };
+        auto est = [&](size_t l, int j) {
+            auto it = memo[l].find(j);
+            if (it != memo[l].end()) return it->second;
+            const double e = enc[l]->estimate_at(j);
+            memo[l][j] = e;
+            return e;
+        };
+        auto total = [&](int t) {
+            double e = 0.0;
+            for (size_t l = 0; l < nl; l++) e += (double)(layers[l].rows * layers[l].cols) * est(l, j_of(l, t));
+            return e;
+        };
+        const double budget = (double)avg_bpp * n_total;
+        int t_lo = INT32_MAX, t_hi = INT32_MIN;
+        for (size_t l = 0; l < nl; l++) {
+            t_lo = std::min(t_lo, jmin[l] + off[l]);
+            t_hi = std::max(t_hi, ep::kJMax + off[l]);
+        }
+        int t;
+        if (total(t_lo) <= budget) {
+            t = t_lo;
+        } else if (total(t_hi) > budget) {
+            t = t_hi;
+        } else {
+            int lo = t_lo, hi = t_hi;  // total(lo) > budget >= total(hi)
+            while (hi - lo > 1) {
+                const int mid = lo + (hi - lo) / 2;
+                (total(mid) <= budget ? hi : lo) = mid;
+            }
+            t = hi;
+        }
+        for (size_t l = 0; l < nl; l++) {
+            j_out[l] = j_of(l, t);
+            if (est_bpp_out) est_bpp_out[l] = est(l, j_out[l]);
+        }
+        if (t_out) *t_out = t;
+        return EP_OK;
     } catch (const std::bad_alloc&) {
         return EP_ERR_NOMEM;
     }

@@ -10,8 +10,9 @@
 //   warp 1       allocates 512 TMEM columns and issues tcgen05.mma
 //                (M = 128 tokens, N = 256 weight rows, K = 16 per instruction,
 //                fp32 accumulators) into two alternating 256-column buffers
-//   warps 2..5   epilogue: tcgen05.ld of the finished accumulator, BF16
-//                rounding, 16-byte stores of Y, then release of the buffer,
+//   warps 2..5   epilogue: tcgen05.ld of the finished accumulator, plus the
+//                optional bias in fp32, BF16 rounding, 16-byte stores of Y,
+//                then release of the buffer,
 //                so the epilogue of one tile overlaps the MMAs of the next
 // Output tiles are visited in groups of 16 token tiles (see tile_coords), so
 // the CTAs running at the same time share a few W row-slabs and the group's
@@ -72,7 +73,8 @@ __device__ __forceinline__ void gemm_fail(volatile int* abort_flag, uint32_t* st
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw,
-                     uint16_t* __restrict__ y, const GemmShape sh, uint32_t* status) {
+                     uint16_t* __restrict__ y, const uint16_t* __restrict__ bias, const GemmShape sh,
+                     uint32_t* status) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ volatile int s_abort;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -185,16 +187,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tmem_ld_wait();
                 const int64_t col = (int64_t)n * BN + c * 32;
                 if (row < sh.T && col < sh.N) {
-                    uint32_t p[16];
-#pragma unroll
-                    for (int i = 0; i < 16; i++) {
-                        __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                        p[i] = *reinterpret_cast<uint32_t*>(&h);
-                    }
                     uint4* dst = reinterpret_cast<uint4*>(yrow + col);
 #pragma unroll
-                    for (int i = 0; i < 4; i++)  // 8 columns each; N is a multiple of 8
-                        if (col + 8 * i < sh.N) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+                    for (int i = 0; i < 4; i++) {  // 8 columns each; N is a multiple of 8
+                        if (col + 8 * i >= sh.N) break;
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e++) v[e] = __uint_as_float(r[8 * i + e]);
+                        if (bias) {  // Y = BF16(acc + b): the bias joins the fp32 sum before the one rounding
+                            const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias + col + 8 * i));
+                            const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                            for (int e = 0; e < 4; e++) {
+                                v[2 * e] += __uint_as_float(bw[e] << 16);
+                                v[2 * e + 1] += __uint_as_float(bw[e] & 0xFFFF0000u);
+                            }
+                        }
+                        uint32_t p[4];
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+                            p[e] = *reinterpret_cast<uint32_t*>(&h);
+                        }
+                        dst[i] = make_uint4(p[0], p[1], p[2], p[3]);
+                    }
                 }
             }
             tc_fence_before_sync();
@@ -252,8 +268,8 @@ int sm_count() {
     return cache[dev] ? cache[dev] : 148;
 }
 
-ep_status gemm_launch(const uint16_t* d_x, const uint16_t* d_w, uint16_t* d_y, int64_t T, int64_t N, int64_t K,
-                      uint32_t* d_status, cudaStream_t stream) {
+ep_status gemm_launch(const uint16_t* d_x, const uint16_t* d_w, uint16_t* d_y, const uint16_t* d_bias, int64_t T,
+                      int64_t N, int64_t K, uint32_t* d_status, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
@@ -272,16 +288,16 @@ ep_status gemm_launch(const uint16_t* d_x, const uint16_t* d_w, uint16_t* d_y, i
     sh.kblocks = (int)((K + BK - 1) / BK);
     const int tiles = sh.tiles_m * sh.tiles_n;
     const int grid = tiles < sm_count() ? tiles : sm_count();
-    gemm_bf16_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(tx, tw, d_y, sh, d_status);
+    gemm_bf16_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(tx, tw, d_y, d_bias, sh, d_status);
     return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-ep_status check_gemm_args(const void* d_x, const void* d_w, const void* d_y, int64_t T, int64_t N, int64_t K,
-                          const uint32_t* d_status) {
+ep_status check_gemm_args(const void* d_x, const void* d_w, const void* d_y, const void* d_bias, int64_t T, int64_t N,
+                          int64_t K, const uint32_t* d_status) {
     if (!d_x || !d_w || !d_y || !d_status) return EP_ERR_INVALID_ARG;
-    if (!aligned16(d_x) || !aligned16(d_w) || !aligned16(d_y)) return EP_ERR_INVALID_ARG;
+    if (!aligned16(d_x) || !aligned16(d_w) || !aligned16(d_y) || !aligned16(d_bias)) return EP_ERR_INVALID_ARG;
     if (T <= 0 || N <= 0 || K <= 0) return EP_ERR_SHAPE;
     if (N % 8 || K % 8) return EP_ERR_SHAPE;
     if (T > ((int64_t)1 << 31) - BM || N > ((int64_t)1 << 31) - BN || K > ((int64_t)1 << 31)) return EP_ERR_SHAPE;
@@ -293,18 +309,18 @@ ep_status check_gemm_args(const void* d_x, const void* d_w, const void* d_y, int
 
 extern "C" {
 
-ep_status ep_linear_bf16(const uint16_t* d_x, const uint16_t* d_w, uint16_t* d_y, int64_t tokens, int64_t rows,
-                         int64_t cols, uint32_t* d_status, ep_stream_t stream) {
-    ep_status st = ep::check_gemm_args(d_x, d_w, d_y, tokens, rows, cols, d_status);
+ep_status ep_linear_bf16(const uint16_t* d_x, const uint16_t* d_w, uint16_t* d_y, const uint16_t* d_bias,
+                         int64_t tokens, int64_t rows, int64_t cols, uint32_t* d_status, ep_stream_t stream) {
+    ep_status st = ep::check_gemm_args(d_x, d_w, d_y, d_bias, tokens, rows, cols, d_status);
     if (st != EP_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(d_status, 0, sizeof(uint32_t), s) != cudaSuccess) return EP_ERR_CUDA;
-    return ep::gemm_launch(d_x, d_w, d_y, tokens, rows, cols, d_status, s);
+    return ep::gemm_launch(d_x, d_w, d_y, d_bias, tokens, rows, cols, d_status, s);
 }
 
 ep_status ep_compressed_linear(const uint8_t* h_blob, const void* d_blob, size_t bytes, const uint16_t* d_x,
-                               int64_t tokens, uint16_t* d_y, int32_t mode, void* d_ws, size_t ws_bytes,
-                               uint32_t* d_status, ep_stream_t stream) {
+                               int64_t tokens, uint16_t* d_y, const uint16_t* d_bias, int32_t mode, void* d_ws,
+                               size_t ws_bytes, uint32_t* d_status, ep_stream_t stream) {
     using namespace ep;
     if (!h_blob || !d_blob || !d_status) return EP_ERR_INVALID_ARG;
     ep_info info;
@@ -314,13 +330,13 @@ ep_status ep_compressed_linear(const uint8_t* h_blob, const void* d_blob, size_t
     if (mode != EP_LINEAR_DECODE_THEN_GEMM) return EP_ERR_UNSUPPORTED;
     const size_t need = (size_t)info.rows * (size_t)info.cols * 2u;
     if (!d_ws || ws_bytes < need) return EP_ERR_INVALID_ARG;
-    st = check_gemm_args(d_x, d_ws, d_y, tokens, info.rows, info.cols, d_status);
+    st = check_gemm_args(d_x, d_ws, d_y, d_bias, tokens, info.rows, info.cols, d_status);
     if (st != EP_OK) return st;
     // ep_decode zeroes the status word, decodes W into the workspace, and the
     // GEMM (same stream) reads it back, mostly from L2
     st = ep_decode(h_blob, d_blob, bytes, d_ws, nullptr, d_status, stream);
     if (st != EP_OK) return st;
-    return gemm_launch(d_x, static_cast<const uint16_t*>(d_ws), d_y, tokens, info.rows, info.cols, d_status,
+    return gemm_launch(d_x, static_cast<const uint16_t*>(d_ws), d_y, d_bias, tokens, info.rows, info.cols, d_status,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -15,7 +15,8 @@
  * Checks", sections "Choose a compression contract" (lossy target bitrate vs
  * lossless tiled ANS; compress / decompress), "Start with a tensor round trip"
  * (target_bpp vs actual_bpp, which includes metadata).
- * The byte layout is fixed in FORMAT.md (version 1).
+ * The byte layout is stream format version 1 (header, tables, tile offsets,
+ * 4-lane tile payloads).
  *
  * Conventions
  *  - Matrices are row-major; rows = out_features (M), cols = in_features (K).
@@ -114,6 +115,53 @@ ep_status ep_encode(const void *w, int64_t rows, int64_t cols, const ep_params *
                     size_t *blob_bytes);
 void ep_free(void *p);
 
+/*
+ * Lossy encode at a caller-chosen resolution index j (Delta = 2^(j/64)), with
+ * no rate search; otherwise as ep_encode (p->mode must be EP_MODE_LOSSY_E8;
+ * p->target_bpp is only recorded in the header).  EP_ERR_INVALID_ARG when j
+ * is outside [-640, 128] or below the smallest index that keeps every row's
+ * peak in range (ep_estimate_bpp reports that index).
+ */
+ep_status ep_encode_at(const void *w, int64_t rows, int64_t cols, const ep_params *p, int32_t j, uint8_t **blob,
+                       size_t *blob_bytes);
+
+/*
+ * The sampled storage estimate ("Sampled storage estimates select the
+ * quantization resolution without repeated full-stream encoding", Abstract)
+ * of a BF16 matrix (host) at index j: coded bits per parameter on the strided
+ * row sample (sample_frac <= 0 selects 0.05), the figure the rate search
+ * steers.  *j_min (may be NULL) receives the smallest admissible index.
+ */
+ep_status ep_estimate_bpp(const uint16_t *w, int64_t rows, int64_t cols, float sample_frac, int32_t j,
+                          int32_t n_threads, double *bpp, int32_t *j_min);
+
+/* One layer of a model-level allocation: a BF16 matrix in host memory. */
+typedef struct {
+    const uint16_t *w;
+    int64_t rows, cols; /* cols % 8 == 0 */
+    float sensitivity;  /* alpha > 0: weight of this layer's squared relative error (1 = neutral) */
+} ep_layer_ref;
+
+/*
+ * Per-layer bitrate allocation for a whole-model budget ("EntroPack PyTorch
+ * Guide", "Separate reconstruction metrics from application metrics":
+ * different bitrates across layers, with the allocation recorded).  Minimises
+ * sum_l alpha_l n_l D_l subject to sum_l n_l R_l <= avg_bpp * sum_l n_l.  At
+ * high resolution every row-normalised layer has D ~ Delta^2, so the optimum
+ * has equal slopes, alpha_l Delta_l^2 constant:
+ *   o_l = lround(32 log2 alpha_l),  j_l(t) = clamp(t - o_l, j_min_l, 128);
+ *   t = the smallest shared index whose estimated total
+ *       E(t) = sum_l n_l * estimate_l(j_l(t)) fits the budget, by bisection
+ *       between min_l(j_min_l + o_l) and max_l(128 + o_l) (the lower end if it
+ *       fits, the upper end if nothing fits).
+ * Writes j_out[n_layers] (encode each layer with ep_encode_at), optionally
+ * est_bpp_out[n_layers] and *t_out.  Errors: EP_ERR_INVALID_ARG (NULL, no
+ * layers, sensitivity not positive and finite, bad budget), EP_ERR_SHAPE,
+ * EP_ERR_NONFINITE, EP_ERR_NOMEM.
+ */
+ep_status ep_allocate_bits(const ep_layer_ref *layers, int64_t n_layers, float avg_bpp, float sample_frac,
+                           int32_t n_threads, int32_t *j_out, double *est_bpp_out, int32_t *t_out);
+
 /* 8 * bytes / (rows * cols) after validating the stream ("actual_bpp", metadata included). */
 ep_status ep_actual_bpp(const uint8_t *blob, size_t bytes, double *bpp);
 /* Parse and fully validate a host copy of a stream. */
@@ -187,11 +235,13 @@ ep_status ep_batch_decode(const ep_batch_plan *plan, uint32_t *d_status, ep_stre
 
 /*
  * Linear layers ("EntroPack PyTorch Guide", "Replace one linear layer before
- * a whole model": CompressedLinear.from_linear).  Y = X * W^T with row-major
- * BF16 X [tokens x cols], W [rows x cols] and Y [tokens x rows]; the product
- * is accumulated in fp32 by tcgen05 tensor-core instructions and rounded to
- * BF16 once.  Device pointers are caller-owned and 16-byte aligned; tokens
- * may be any positive count, rows and cols must be multiples of 8.
+ * a whole model": CompressedLinear.from_linear).  Y = X * W^T (+ b) with
+ * row-major BF16 X [tokens x cols], W [rows x cols], Y [tokens x rows] and an
+ * optional BF16 bias b [rows] (NULL: none); the product is accumulated in
+ * fp32 by tcgen05 tensor-core instructions, the bias is added in fp32, and
+ * the sum is rounded to BF16 once.  Device pointers are caller-owned and
+ * 16-byte aligned; tokens may be any positive count, rows and cols must be
+ * multiples of 8.
  * d_status (one u32) is zeroed by the call; the kernel sets
  * EP_STATUS_WAIT_TIMEOUT if an internal pipeline wait gives up (about 2 s),
  * which never happens in a correct run.  Returns EP_OK once enqueued.
@@ -202,8 +252,8 @@ typedef enum {
 } ep_linear_mode;
 
 /* Dense BF16 GEMM (uncompressed W): the tensor-core kernel used by ep_compressed_linear. */
-ep_status ep_linear_bf16(const uint16_t *d_x, const uint16_t *d_w, uint16_t *d_y, int64_t tokens, int64_t rows,
-                         int64_t cols, uint32_t *d_status, ep_stream_t stream);
+ep_status ep_linear_bf16(const uint16_t *d_x, const uint16_t *d_w, uint16_t *d_y, const uint16_t *d_bias,
+                         int64_t tokens, int64_t rows, int64_t cols, uint32_t *d_status, ep_stream_t stream);
 
 /*
  * CompressedLinear forward on a lossy BF16 stream (h_blob / d_blob as for
@@ -215,8 +265,8 @@ ep_status ep_linear_bf16(const uint16_t *d_x, const uint16_t *d_w, uint16_t *d_y
  * stream, or a mode this build does not provide).
  */
 ep_status ep_compressed_linear(const uint8_t *h_blob, const void *d_blob, size_t bytes, const uint16_t *d_x,
-                               int64_t tokens, uint16_t *d_y, int32_t mode, void *d_ws, size_t ws_bytes,
-                               uint32_t *d_status, ep_stream_t stream);
+                               int64_t tokens, uint16_t *d_y, const uint16_t *d_bias, int32_t mode, void *d_ws,
+                               size_t ws_bytes, uint32_t *d_status, ep_stream_t stream);
 
 /*
  * Allocation-free variant of ep_batch_prepare + ep_batch_decode.  The pages
@@ -245,6 +295,47 @@ ep_status ep_compressed_linear(const uint8_t *h_blob, const void *d_blob, size_t
 #define EP_BATCH_STATIC_MAX_ITEMS 1024
 ep_status ep_batch_decode_static(const ep_batch_item *items, int64_t n_items, int32_t ring, uint32_t *d_status,
                                  ep_stream_t stream);
+
+/* ---- Fixed-width 4-bit comparators (NF4, INT4) ----------------------------
+ * The formats EntroPack is evaluated against ("EntroPack: Fast and Accurate
+ * Entropy-Coded Weight Compression at Arbitrary Bitrates", Abstract: about 24%
+ * lower relative L2 weight error than NF4 at a 4-bit target, with less
+ * storage).  Block-absmax 4-bit codebook quantisation:
+ *  - the n weights (BF16, any row-major order; n even) form blocks of `block`
+ *    consecutive weights (block a multiple of 16; the last block may be short);
+ *  - each block stores s = max |w| as FP32 (scales[n / block rounded up]);
+ *  - each weight stores the 4-bit code k minimising |w / s - levels[k]| (FP32
+ *    arithmetic, ties to the lower k; w / s = 0 when s = 0), packed two per
+ *    byte, element 2j in the low nibble of codes[j] (n / 2 bytes);
+ *  - reconstruction is BF16(levels[k] * s): one FP32 product, round to
+ *    nearest even.  Storage: 4 + 32 / block bits per weight.
+ * NF4 levels: standard-normal quantiles at 7 negative and 8 positive evenly
+ * spaced probabilities from 1 - d down towards 1/2 (d = (1/32 + 1/30) / 2)
+ * plus an exact zero, scaled to [-1, 1], ascending.  INT4 levels: k / 7 for
+ * k = -7..7 (index k + 7) and a 16th code equal to 0 that is never chosen. */
+typedef enum { EP_Q4_NF4 = 0, EP_Q4_INT4 = 1 } ep_q4_kind;
+
+/* Host: the 16 FP32 levels of `kind` into levels[16].  EP_ERR_INVALID_ARG on a
+ * bad kind or NULL. */
+ep_status ep_q4_levels(int32_t kind, float *levels);
+
+/* Host: quantise n BF16 weights w (host memory) with levels[16] into codes
+ * (n / 2 bytes) and scales (FP32, ceil(n / block)); all caller-owned host
+ * buffers.  n_threads <= 0 uses every hardware thread; the result does not
+ * depend on it.  Errors: EP_ERR_INVALID_ARG (NULL, block not a positive
+ * multiple of 16, non-finite level), EP_ERR_SHAPE (n <= 0 or odd),
+ * EP_ERR_NONFINITE (a weight is NaN or +-inf). */
+ep_status ep_q4_encode(const uint16_t *w, int64_t n, int64_t block, const float *levels, uint8_t *codes,
+                       float *scales, int32_t n_threads);
+
+/* Device: reconstruct the n BF16 weights into d_out (n x 2 bytes) from d_codes
+ * (8-byte aligned) and d_scales (device), with levels[16] read from HOST
+ * memory at the call.  Asynchronous on `stream`; allocates nothing.  Errors
+ * before launch: EP_ERR_INVALID_ARG (NULL, misaligned: d_out needs 16 bytes,
+ * d_scales 4; bad block), EP_ERR_SHAPE (n <= 0 or odd); EP_ERR_CUDA if the
+ * launch fails. */
+ep_status ep_q4_decode(const uint8_t *d_codes, const float *d_scales, int64_t n, int64_t block, const float *levels,
+                       uint16_t *d_out, ep_stream_t stream);
 
 /* Synchronise `stream` and map the status word: 0 -> EP_OK, any bit -> EP_ERR_CORRUPT. */
 ep_status ep_sync_status(const uint32_t *d_status, ep_stream_t stream);

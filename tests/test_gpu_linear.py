@@ -33,12 +33,16 @@ def _bf16_dev(bits: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).cuda()
 
 
-def _check(y: torch.Tensor, x_bits: np.ndarray, w64: np.ndarray, rows=None):
+def _check(y: torch.Tensor, x_bits: np.ndarray, w64: np.ndarray, rows=None, bias_bits=None):
     x64 = synth.bf16_to_f32(x_bits).astype(np.float64)
     if rows is not None:
         x64 = x64[rows]
     y_ref = oracle.gemm_f64(x64, w64)
     mag = oracle.gemm_f64(np.abs(x64), np.abs(w64))
+    if bias_bits is not None:  # one more fp32 addend before the single rounding
+        b64 = synth.bf16_to_f32(bias_bits).astype(np.float64)
+        y_ref = y_ref + b64
+        mag = mag + np.abs(b64)
     yg = y.float().cpu().numpy().astype(np.float64)
     if rows is not None:
         yg = yg[rows]
@@ -55,6 +59,23 @@ def test_dense_gemm_ragged(ep, T, N, K):
     w = synth.student_t5_bf16(200 + N, N, K)
     y = ep.linear_bf16(_bf16_dev(x), _bf16_dev(w))
     _check(y, x, synth.bf16_to_f32(w).astype(np.float64))
+
+
+@pytest.mark.parametrize("T,N,K", [(300, 544, 200), (77, 1000, 1000)])
+def test_bias_in_epilogue(ep, T, N, K):
+    x = synth.normal_bf16(300 + T, T, K, std=1.0)
+    w = synth.student_t5_bf16(400 + N, N, K)
+    b = synth.normal_bf16(500 + N, 1, N, std=0.5)[0]
+    bd = torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    y = ep.linear_bf16(_bf16_dev(x), _bf16_dev(w), bias=bd)
+    _check(y, x, synth.bf16_to_f32(w).astype(np.float64), bias_bits=b)
+    blob = oracle.encode(w, 4.0)
+    yc = ep.compressed_linear(ep.DeviceBlob(blob), _bf16_dev(x), bias=bd)
+    _check(yc, x, oracle.container_to_f64(oracle.decode(blob)[0], "bf16"), bias_bits=b)
+    # a zero bias changes no value (only -0 may become +0)
+    y0 = ep.linear_bf16(_bf16_dev(x), _bf16_dev(w))
+    y1 = ep.linear_bf16(_bf16_dev(x), _bf16_dev(w), bias=torch.zeros_like(bd))
+    assert torch.equal(y0.float(), y1.float())
 
 
 def test_dense_gemm_matches_torch_closely(ep):
@@ -123,6 +144,40 @@ def test_compressed_linear_module(ep):
     x = torch.randn(2, 50, 1024).to(torch.bfloat16).cuda()
     y = cl(x)
     assert y.shape == (2, 50, 512)
-    w_hat = torch.from_numpy(oracle.container_to_f64(oracle.decode(oracle.encode(w, 4.0))[0], "bf16")).cuda()
-    ref = x.double() @ w_hat.t() + lin.bias.detach().double().cuda()
-    assert ((y.double() - ref).abs().max() / ref.abs().max()).item() < 2e-2
+    w_hat = oracle.container_to_f64(oracle.decode(oracle.encode(w, 4.0))[0], "bf16")
+    b_bits = lin.bias.detach().to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    x_bits = x.reshape(-1, 1024).cpu().view(torch.int16).numpy().view(np.uint16)
+    _check(y.reshape(-1, 512), x_bits, w_hat, bias_bits=b_bits)
+
+
+def test_compress_linears_with_allocation(ep):
+    """Three layers under one 3.5-bit budget: each forward matches the oracle's decode at its allocated index."""
+    torch.manual_seed(1)
+    shapes = {"attn.q": (256, 512), "ffn.up": (1024, 512), "ffn.down": (512, 1024)}
+    gens = {"attn.q": synth.normal_bf16, "ffn.up": synth.student_t5_bf16, "ffn.down": synth.student_t5_bf16}
+    lins, bits = {}, {}
+    for i, (k, (n, kk)) in enumerate(shapes.items()):
+        bits[k] = gens[k](70 + i, n, kk)
+        lin = torch.nn.Linear(kk, n, bias=(k != "ffn.down"))
+        with torch.no_grad():
+            lin.weight.copy_(torch.from_numpy(synth.bf16_to_f32(bits[k])))
+        lins[k] = lin
+    sens = {"attn.q": 4.0}
+    cls, record = ep.compress_linears(lins, 3.5, sens)
+    plan = oracle.allocate_bits([bits[k] for k in shapes], 3.5, [sens.get(k, 1.0) for k in shapes])
+    assert [record["layers"][k]["j"] for k in shapes] == plan["j"]
+    assert record["layers"]["attn.q"]["j"] == plan["t"] - 64
+    for k, (n, kk) in shapes.items():
+        blob = oracle.encode_at(bits[k], plan["j"][list(shapes).index(k)],
+                                record["layers"][k]["est_bpp"])
+        assert cls[k].ct.blob.host.numpy().tobytes() == blob
+        x_bits = synth.normal_bf16(80, 100, kk, std=1.0)
+        y = cls[k](_bf16_dev(x_bits))
+        w_hat = oracle.container_to_f64(oracle.decode(blob)[0], "bf16")
+        if lins[k].bias is None:
+            _check(y, x_bits, w_hat)
+        else:
+            b = lins[k].bias.detach().to(torch.bfloat16).double().numpy()
+            ref = oracle.gemm_f64(synth.bf16_to_f32(x_bits).astype(np.float64), w_hat) + b
+            err = np.abs(y.double().cpu().numpy() - ref).max() / np.abs(ref).max()
+            assert err < 2e-2

@@ -167,3 +167,109 @@ def test_device_entry_points_validate_before_launch():
     assert lib.ep_sync_status(None, None) == 1
     assert lib.ep_batch_workspace_bytes(0) == 0
     assert lib.ep_batch_workspace_bytes(5) > 0
+
+
+# --------------------------------------------- fixed-width 4-bit comparators
+@pytest.mark.parametrize("kind", ["nf4", "int4"])
+def test_q4_levels_match_oracle(kind):
+    ep = _ep()
+    lv = ep.q4_levels(kind)
+    np.testing.assert_array_equal(lv.view(np.uint32), oracle.q4_levels(kind).astype(np.float32).view(np.uint32))
+
+
+@pytest.mark.parametrize("kind", ["nf4", "int4"])
+@pytest.mark.parametrize("shape,block", [((64, 1024), 64), ((45, 200), 16), ((3, 136), 128), ((1, 8), 16),
+                                         ((33, 1000), 1024)])
+def test_q4_encoder_byte_identical(kind, shape, block):
+    ep = _ep()
+    w = synth.rows_outliers_bf16(shape[0] + block, *shape)
+    w[0, :4] = 0
+    q = ep.q4_encode(w, kind, block)
+    codes, scales, _, bits = oracle.q4_roundtrip(w, kind, block)
+    flat = codes.reshape(-1)
+    np.testing.assert_array_equal(q.codes, (flat[0::2] | (flat[1::2] << 4)).astype(np.uint8))
+    np.testing.assert_array_equal(q.scales.view(np.uint32), scales.view(np.uint32))
+    assert q.bits_per_weight == pytest.approx(bits, abs=32.0 / w.size)
+    for t in (1, 3):
+        q2 = ep.q4_encode(w, kind, block, n_threads=t)
+        assert (q2.codes == q.codes).all() and (q2.scales == q.scales).all()
+
+
+def test_q4_errors():
+    ep = _ep()
+    from dit_weight_compression_02_b300._lib import lib
+    w = synth.normal_bf16(40, 4, 64)
+    with pytest.raises(ep.EntroPackError) as e:
+        ep.q4_encode(w, "nf4", block=24)
+    assert e.value.status == "EP_ERR_INVALID_ARG"
+    bad = w.copy()
+    bad[1, 5] = 0x7FC0  # NaN
+    with pytest.raises(ep.EntroPackError) as e:
+        ep.q4_encode(bad)
+    assert e.value.status == "EP_ERR_NONFINITE"
+    with pytest.raises(ep.EntroPackError) as e:
+        ep.q4_encode(w.reshape(-1)[:7].copy())
+    assert e.value.status == "EP_ERR_SHAPE"
+    lv = np.zeros(16, np.float32)
+    assert lib.ep_q4_levels(2, lv.ctypes.data) == 1
+    # device entry point: argument errors return before any CUDA call
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.ep_q4_decode(fake, fake, 64, 64, lv.ctypes.data, ctypes.c_void_p((1 << 20) + 8), None) == 1
+    assert lib.ep_q4_decode(ctypes.c_void_p((1 << 20) + 4), fake, 64, 64, lv.ctypes.data, fake, None) == 1
+    assert lib.ep_q4_decode(fake, fake, 63, 64, lv.ctypes.data, fake, None) == 2
+    assert lib.ep_q4_decode(fake, fake, 64, 8, lv.ctypes.data, fake, None) == 1
+    assert lib.ep_q4_decode(fake, fake, 64, 64, None, fake, None) == 1
+
+
+# ------------------------------------------------ per-layer bit allocation
+def _alloc_layers():
+    return [synth.student_t5_bf16(51, 64, 256), synth.normal_bf16(52, 45, 200),
+            synth.rows_outliers_bf16(53, 32, 1024, frac=0.01, k_sigma=12.0)]
+
+
+@pytest.mark.parametrize("sens", [None, [4.0, 1.0, 0.25], [2.0, 3.0, 0.7]])
+@pytest.mark.parametrize("avg", [2.5, 4.0, 20.0, 0.01])
+def test_allocation_identical_to_oracle(sens, avg):
+    ep = _ep()
+    layers = _alloc_layers()
+    r_lib = ep.allocate_bits(layers, avg, sens)
+    r_orc = oracle.allocate_bits(layers, avg, sens)
+    assert r_lib["t"] == r_orc["t"] and r_lib["j"] == r_orc["j"]
+    assert r_lib["est_bpp"] == r_orc["est_bpp"]  # bit-identical estimates
+
+
+def test_estimate_and_encode_at_identical_to_oracle():
+    ep = _ep()
+    for w in _alloc_layers():
+        jmin = oracle.smallest_valid_j(w)
+        for j in (jmin, jmin + 37, 0, 128):
+            bpp, jm = ep.estimate_bpp(w, j)
+            assert jm == jmin and bpp == oracle.estimate_bpp(w, 0.05, j)
+            assert ep.encode(w, 3.25, j=j) == oracle.encode_at(w, j, 3.25)
+        for c in ("fp8", "int8"):
+            assert ep.encode(w, 3.0, c, j=jmin + 64) == oracle.encode_at(w, jmin + 64, 3.0, c)
+
+
+def test_allocation_errors():
+    ep = _ep()
+    layers = _alloc_layers()
+    for sens in ([1.0, 0.0, 1.0], [1.0, -2.0, 1.0], [1.0, float("inf"), 1.0]):
+        with pytest.raises(ep.EntroPackError) as e:
+            ep.allocate_bits(layers, 4.0, sens)
+        assert e.value.status == "EP_ERR_INVALID_ARG"
+    with pytest.raises(ep.EntroPackError) as e:
+        ep.allocate_bits(layers, 0.0)
+    assert e.value.status == "EP_ERR_INVALID_ARG"
+    bad = layers[0].copy()
+    bad[2, 2] = 0x7F80
+    with pytest.raises(ep.EntroPackError) as e:
+        ep.allocate_bits([bad, layers[1]], 4.0)
+    assert e.value.status == "EP_ERR_NONFINITE"
+    with pytest.raises(ep.EntroPackError) as e:
+        ep.allocate_bits([layers[0][:, :100].copy()], 4.0)
+    assert e.value.status == "EP_ERR_SHAPE"
+    jmin = oracle.smallest_valid_j(layers[0])
+    for j in (jmin - 1, 129, -641):
+        with pytest.raises(ep.EntroPackError) as e:
+            ep.encode(layers[0], 4.0, j=j)
+        assert e.value.status == "EP_ERR_INVALID_ARG"
