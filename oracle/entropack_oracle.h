@@ -23,9 +23,8 @@
  * second moment 929/12960, rANS round trip and code-length bounds,
  * conversions against torch, the Gaussian rate-distortion closed form,
  * bitwise lossless recovery, NF4 levels through the normal CDF, brute-force
- * 4-bit quantisation, E4M3 decoding against torch.  Parity unpinned: the exact resolution index
- * chosen by the rate search (only its determinism and its distance to the
- * target are pinned).
+ * 4-bit quantisation, E4M3 decoding against torch, the rate search's chosen
+ * resolution index against an exhaustive scan of every admissible index.
  */
 #ifndef ENTROPACK_ORACLE_H
 #define ENTROPACK_ORACLE_H

@@ -137,6 +137,30 @@ def test_rate_search_is_locally_best():
         assert oracle.select_j(w, target, 0.05) == (j, jlo)
 
 
+@pytest.mark.parametrize("gen,target", [("normal", 3.0), ("student_t5", 4.0), ("rows_outliers", 2.5)])
+def test_rate_search_by_exhaustive_scan(gen, target):
+    """The resolution the search picks, against a scan of every admissible index.
+
+    Where "estimate(j) <= target" switches from false to true exactly once as
+    j grows (checked here: the estimate itself wobbles only at escape-heavy
+    resolutions near 16 bits, far above any target), the crossing is unique,
+    and the search must return whichever of the two indices around it has the
+    estimate closer to the target (ties to the coarser one).
+    """
+    w = getattr(synth, f"{gen}_bf16")(61, 64, 512)
+    j, jlo = oracle.select_j(w, target, 0.25)
+    assert jlo == oracle.smallest_valid_j(w)
+    js = list(range(jlo, 129))
+    est = [oracle.estimate_bpp(w, 0.25, x) for x in js]
+    fit = [x for x, e in zip(js, est) if e <= target]
+    assert fit and fit[0] > jlo
+    hi = fit[0]
+    assert fit == list(range(hi, 129)), "the target is crossed more than once for this case"
+    e_hi, e_lo = est[hi - jlo], est[hi - 1 - jlo]
+    expect = hi if abs(e_hi - target) <= abs(e_lo - target) else hi - 1
+    assert j == expect
+
+
 def test_zero_rows_and_constant_rows():
     w = _w(4, 64, 256)
     w[3] = 0
