@@ -739,13 +739,12 @@ size_t batch_layout(int64_t n, size_t* items_off, size_t* units_off, size_t* ctr
     return batch_bytes(n);
 }
 
-ep_status fill_args(const uint8_t* h_blob, const void* d_blob, size_t bytes, void* d_out, float* d_scale,
-                    uint8_t* d_sym, uint32_t* d_status, Layout& L, DecodeArgs* a) {
-    if (!h_blob || !d_blob || !d_out) return EP_ERR_INVALID_ARG;
+// kernel arguments of a stream already parsed and validated into L
+ep_status fill_args_parsed(const Layout& L, const void* d_blob, void* d_out, float* d_scale, uint8_t* d_sym,
+                           uint32_t* d_status, DecodeArgs* a) {
+    if (!d_blob || !d_out) return EP_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(d_blob) | reinterpret_cast<uintptr_t>(d_out)) & 15u) return EP_ERR_INVALID_ARG;
     if (d_sym && (reinterpret_cast<uintptr_t>(d_sym) & 7u)) return EP_ERR_INVALID_ARG;
-    ep_status st = parse_and_validate(h_blob, bytes, &L);
-    if (st != EP_OK) return st;
     std::memset(a, 0, sizeof(*a));
     const uint8_t* db = static_cast<const uint8_t*>(d_blob);
     a->blob = db;
@@ -766,6 +765,16 @@ ep_status fill_args(const uint8_t* h_blob, const void* d_blob, size_t bytes, voi
     a->n_tiles = L.n_tiles;
     a->tiles_per_row = L.cols_p / kTileCols;
     return EP_OK;
+}
+
+ep_status fill_args(const uint8_t* h_blob, const void* d_blob, size_t bytes, void* d_out, float* d_scale,
+                    uint8_t* d_sym, uint32_t* d_status, Layout& L, DecodeArgs* a) {
+    if (!h_blob || !d_blob || !d_out) return EP_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(d_blob) | reinterpret_cast<uintptr_t>(d_out)) & 15u) return EP_ERR_INVALID_ARG;
+    if (d_sym && (reinterpret_cast<uintptr_t>(d_sym) & 7u)) return EP_ERR_INVALID_ARG;
+    ep_status st = parse_and_validate(h_blob, bytes, &L);
+    if (st != EP_OK) return st;
+    return fill_args_parsed(L, d_blob, d_out, d_scale, d_sym, d_status, a);
 }
 
 int kind_of(const Layout& L) {
@@ -799,16 +808,9 @@ ep_status launch_batch(const ep_batch_plan* p, uint32_t* d_status, cudaStream_t 
     return p->reserved ? launch_batch_r<KIND, true>(p, d_status, stream) : launch_batch_r<KIND, false>(p, d_status, stream);
 }
 
-ep_status decode_impl(const uint8_t* h_blob, const void* d_blob, size_t bytes, void* d_out, float* d_scale,
-                      uint8_t* d_sym, uint32_t* d_status, cudaStream_t stream) {
-    if (!d_status) return EP_ERR_INVALID_ARG;
-    thread_local Layout L;
-    DecodeArgs a;
-    ep_status st = fill_args(h_blob, d_blob, bytes, d_out, d_scale, d_sym, d_status, L, &a);
-    if (st != EP_OK) return st;
+ep_status launch_parsed(const Layout& L, const DecodeArgs& a, bool dump, uint32_t* d_status, cudaStream_t stream) {
     if (cudaMemsetAsync(d_status, 0, sizeof(uint32_t), stream) != cudaSuccess) return EP_ERR_CUDA;
     const size_t smem = decode_smem_bytes(L.n_ctx);
-    const bool dump = d_sym != nullptr;
     switch (kind_of(L)) {
         case K_BF16: return dump ? launch<K_BF16, true>(a, smem, stream) : launch<K_BF16, false>(a, smem, stream);
         case K_FP16: return dump ? launch<K_FP16, true>(a, smem, stream) : launch<K_FP16, false>(a, smem, stream);
@@ -822,7 +824,26 @@ ep_status decode_impl(const uint8_t* h_blob, const void* d_blob, size_t bytes, v
     }
 }
 
+ep_status decode_impl(const uint8_t* h_blob, const void* d_blob, size_t bytes, void* d_out, float* d_scale,
+                      uint8_t* d_sym, uint32_t* d_status, cudaStream_t stream) {
+    if (!d_status) return EP_ERR_INVALID_ARG;
+    thread_local Layout L;
+    DecodeArgs a;
+    ep_status st = fill_args(h_blob, d_blob, bytes, d_out, d_scale, d_sym, d_status, L, &a);
+    if (st != EP_OK) return st;
+    return launch_parsed(L, a, d_sym != nullptr, d_status, stream);
+}
+
 }  // namespace
+
+ep_status decode_parsed(const Layout& L, const void* d_blob, void* d_out, float* d_row_scale, uint32_t* d_status,
+                        ep_stream_t stream) {
+    if (!d_status) return EP_ERR_INVALID_ARG;
+    DecodeArgs a;
+    ep_status st = fill_args_parsed(L, d_blob, d_out, d_row_scale, nullptr, d_status, &a);
+    if (st != EP_OK) return st;
+    return launch_parsed(L, a, false, d_status, reinterpret_cast<cudaStream_t>(stream));
+}
 }  // namespace ep
 extern "C" {
 

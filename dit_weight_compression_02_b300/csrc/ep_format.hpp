@@ -56,6 +56,12 @@ struct Layout {
 // per-tile word counts).  Returns EP_OK or EP_ERR_CORRUPT / EP_ERR_INVALID_ARG.
 ep_status parse_and_validate(const uint8_t* blob, size_t bytes, Layout* out);
 
+// Enqueue the decode of a stream that parse_and_validate already accepted into
+// L (ep_decode without a second host parse): d_blob holds the same bytes on
+// the device; d_out and d_blob are 16-byte aligned; d_status is zeroed first.
+ep_status decode_parsed(const Layout& L, const void* d_blob, void* d_out, float* d_row_scale, uint32_t* d_status,
+                        ep_stream_t stream);
+
 inline size_t container_bytes(int container) {
     return container == EP_C_FP32 ? 4 : (container >= EP_C_FP8_E4M3 ? 1 : 2);
 }

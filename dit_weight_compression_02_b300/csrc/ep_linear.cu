@@ -323,20 +323,20 @@ ep_status ep_compressed_linear(const uint8_t* h_blob, const void* d_blob, size_t
                                size_t ws_bytes, uint32_t* d_status, ep_stream_t stream) {
     using namespace ep;
     if (!h_blob || !d_blob || !d_status) return EP_ERR_INVALID_ARG;
-    ep_info info;
-    ep_status st = ep_query(h_blob, bytes, &info);
+    thread_local Layout L;  // parsed and validated once per call
+    ep_status st = parse_and_validate(h_blob, bytes, &L);
     if (st != EP_OK) return st;
-    if (info.mode != EP_MODE_LOSSY_E8 || info.container != EP_C_BF16) return EP_ERR_UNSUPPORTED;
+    if (L.mode != EP_MODE_LOSSY_E8 || L.container != EP_C_BF16) return EP_ERR_UNSUPPORTED;
     if (mode != EP_LINEAR_DECODE_THEN_GEMM) return EP_ERR_UNSUPPORTED;
-    const size_t need = (size_t)info.rows * (size_t)info.cols * 2u;
+    const size_t need = (size_t)L.rows * (size_t)L.cols * 2u;
     if (!d_ws || ws_bytes < need) return EP_ERR_INVALID_ARG;
-    st = check_gemm_args(d_x, d_ws, d_y, d_bias, tokens, info.rows, info.cols, d_status);
+    st = check_gemm_args(d_x, d_ws, d_y, d_bias, tokens, L.rows, L.cols, d_status);
     if (st != EP_OK) return st;
-    // ep_decode zeroes the status word, decodes W into the workspace, and the
+    // the decode zeroes the status word and writes W into the workspace; the
     // GEMM (same stream) reads it back, mostly from L2
-    st = ep_decode(h_blob, d_blob, bytes, d_ws, nullptr, d_status, stream);
+    st = decode_parsed(L, d_blob, d_ws, nullptr, d_status, stream);
     if (st != EP_OK) return st;
-    return gemm_launch(d_x, static_cast<const uint16_t*>(d_ws), d_y, d_bias, tokens, info.rows, info.cols, d_status,
+    return gemm_launch(d_x, static_cast<const uint16_t*>(d_ws), d_y, d_bias, tokens, L.rows, L.cols, d_status,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
