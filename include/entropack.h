@@ -248,7 +248,11 @@ ep_status ep_batch_decode(const ep_batch_plan *plan, uint32_t *d_status, ep_stre
  */
 typedef enum {
     EP_LINEAR_DECODE_THEN_GEMM = 0, /* decode W into d_ws (rows x cols BF16), then the GEMM */
-    EP_LINEAR_FUSED = 1             /* decode W tiles straight into shared memory (no workspace) */
+    EP_LINEAR_FUSED = 1             /* reserved: W tiles decoded straight into shared memory.  Returns
+                                       EP_ERR_UNSUPPORTED: the accumulator holds at most 512 tokens per
+                                       decoded weight, so W would be decoded tokens / 512 times, and the
+                                       decoded tiles in flight exceed shared memory; decoding once into an
+                                       L2-resident workspace is faster */
 } ep_linear_mode;
 
 /* Dense BF16 GEMM (uncompressed W): the tensor-core kernel used by ep_compressed_linear. */
@@ -262,7 +266,7 @@ ep_status ep_linear_bf16(const uint16_t *d_x, const uint16_t *d_w, uint16_t *d_y
  * Stream corruption found by the decoder shows up in d_status like
  * ep_decode's.  Errors before launch: EP_ERR_INVALID_ARG, EP_ERR_SHAPE,
  * EP_ERR_CORRUPT (host validation), EP_ERR_UNSUPPORTED (lossless or non-BF16
- * stream, or a mode this build does not provide).
+ * stream, or a mode the library does not provide: EP_LINEAR_FUSED).
  */
 ep_status ep_compressed_linear(const uint8_t *h_blob, const void *d_blob, size_t bytes, const uint16_t *d_x,
                                int64_t tokens, uint16_t *d_y, const uint16_t *d_bias, int32_t mode, void *d_ws,
