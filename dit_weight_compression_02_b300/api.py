@@ -239,6 +239,66 @@ class BatchDecoder:
         sync_status(self.status, stream)
 
 
+class StreamingDecoder:
+    """Decode streams whose bytes live in pinned host memory, uploading as it goes.
+
+    The streams are taken in chunks of ``chunk`` consecutive items.  Each
+    launch copies chunk k's bytes to the device on a copy stream and decodes
+    chunk k on the compute stream (ep_batch_decode) as soon as they land, so
+    the upload of chunk k + 1 overlaps the decode of chunk k.  Outputs must be
+    distinct within a chunk and may repeat across chunks (decodes of
+    successive chunks run in order on one stream).  The next launch's upload
+    of a chunk waits for the previous launch's decode of it.
+    """
+
+    def __init__(self, blobs, outs, chunk: int = 7):
+        if len(blobs) != len(outs) or not blobs or chunk < 1:
+            raise ValueError("need one output per stream and a positive chunk")
+        self.blobs = list(blobs)
+        dev = self.blobs[0].device.device
+        self.chunks = []
+        for c0 in range(0, len(self.blobs), chunk):
+            idx = list(range(c0, min(c0 + chunk, len(self.blobs))))
+            if len({outs[i].data_ptr() for i in idx}) != len(idx):
+                raise ValueError("outputs must be distinct within a chunk")
+            self.chunks.append((idx, BatchDecoder([self.blobs[i] for i in idx], [outs[i] for i in idx])))
+        self.status = torch.zeros(len(self.chunks), dtype=torch.int32, device=dev)
+        self._any = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.copy_stream = torch.cuda.Stream(device=dev)
+        self._landed = [torch.cuda.Event() for _ in self.chunks]
+        self._decoded = [torch.cuda.Event() for _ in self.chunks]
+        self._launched = False
+
+    @property
+    def upload_bytes(self) -> int:
+        return sum(b.nbytes for b in self.blobs)
+
+    def launch(self, stream=None) -> None:
+        stream = torch.cuda.current_stream() if stream is None else stream
+        for k, (idx, dec) in enumerate(self.chunks):
+            with torch.cuda.stream(self.copy_stream):
+                if self._launched:
+                    self.copy_stream.wait_event(self._decoded[k])  # the previous decode of these bytes is done
+                for i in idx:
+                    self.blobs[i].device.copy_(self.blobs[i].host, non_blocking=True)
+                self._landed[k].record(self.copy_stream)
+            stream.wait_event(self._landed[k])
+            dec.launch(stream, self.status[k:k + 1])
+            self._decoded[k].record(stream)
+        self._launched = True
+
+    def check(self, stream=None) -> None:
+        """Synchronise and raise EntroPackError if any chunk's decode reported corruption."""
+        stream = torch.cuda.current_stream() if stream is None else stream
+        with torch.cuda.stream(stream):
+            torch.amax(self.status, dim=0, keepdim=True, out=self._any)
+        sync_status(self._any, stream)
+
+    def __call__(self, stream=None) -> None:
+        self.launch(stream)
+        self.check(stream)
+
+
 # ------------------------------------------------------------------ linear
 LINEAR_DECODE_THEN_GEMM, LINEAR_FUSED = 0, 1
 
@@ -469,6 +529,7 @@ def compress_linears(linears: dict, avg_bpp: float, sensitivities: dict | None =
 
 
 __all__ = ["encode", "query", "actual_bpp", "DeviceBlob", "decode", "decode_into", "sync_status", "BatchDecoder",
+           "StreamingDecoder",
            "linear_bf16", "compressed_linear", "LINEAR_DECODE_THEN_GEMM", "LINEAR_FUSED",
            "EntroPackLossyConfig", "TileANSConfig", "CompressedTensor", "compress", "decompress",
            "CompressedLinear", "EntroPackError", "CONTAINERS", "CONTAINER_DTYPES",

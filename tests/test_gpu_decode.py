@@ -329,3 +329,23 @@ def test_c3_whole_model_in_bench_configuration(ep):
             y_o, _ = oracle.decode(blobs[i], tr * tpr, (tr + 1) * tpr)
             rows = slice(tr * 32, tr * 32 + 32)
             assert (g[rows] == y_o[rows]).all(), (i, tr)
+
+
+def test_streaming_decoder_uploads_and_decodes(ep):
+    """Chunks upload on a copy stream and decode as they land; outputs reused across chunks."""
+    ws = [synth.student_t5_bf16(90 + i, 256, 1024) for i in range(7)]
+    blobs = [oracle.encode(w, 3.5) for w in ws]
+    dbs = [ep.DeviceBlob(b) for b in blobs]
+    for db in dbs:
+        db.device.zero_()  # the decoder must upload the bytes itself
+    bufs = [torch.empty((256, 1024), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    outs = [bufs[i % 3] for i in range(7)]
+    with pytest.raises(ValueError):
+        ep.StreamingDecoder(dbs, outs, chunk=4)  # buffer 0 twice inside one chunk
+    sd = ep.StreamingDecoder(dbs, outs, chunk=3)
+    for _ in range(3):
+        sd()
+        for k in range(3):
+            last = max(i for i in range(7) if i % 3 == k)
+            assert (_np(bufs[k]) == oracle.decode(blobs[last])[0]).all()
+    assert sd.upload_bytes == sum(len(b) for b in blobs)
