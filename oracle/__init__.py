@@ -113,7 +113,7 @@ def lib():
         L.oracle_e4m3_to_f64.restype = f64
         L.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
         L.oracle_fp8_row_roundtrip.restype = f64
-        L.oracle_fp8_row_roundtrip.argtypes = [P, i64, i64, P]
+        L.oracle_fp8_row_roundtrip.argtypes = [P, i64, i64, P, P, P]
         _lib = L
     return _lib
 
@@ -491,12 +491,17 @@ def e4m3_to_f64(b: int) -> float:
     return lib().oracle_e4m3_to_f64(int(b))
 
 
-def fp8_row_roundtrip(w_bits: np.ndarray):
-    """Per-row-scaled FP8 E4M3 comparator: (BF16 reconstruction bits, bits per weight)."""
+def fp8_row_roundtrip(w_bits: np.ndarray, with_codes: bool = False):
+    """Per-row-scaled FP8 E4M3 comparator: (BF16 reconstruction bits, bits per weight).
+
+    with_codes: also return the E4M3 bytes (M x K) and the FP32 row scales."""
     w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
     recon = np.zeros(w_bits.shape, dtype=np.uint16)
-    bits = lib().oracle_fp8_row_roundtrip(_p(w_bits), w_bits.shape[0], w_bits.shape[1], _p(recon))
-    return recon, bits
+    codes = np.zeros(w_bits.shape, dtype=np.uint8)
+    scales = np.zeros(w_bits.shape[0], dtype=np.float32)
+    bits = lib().oracle_fp8_row_roundtrip(_p(w_bits), w_bits.shape[0], w_bits.shape[1], _p(recon), _p(codes),
+                                          _p(scales))
+    return (recon, bits, codes, scales) if with_codes else (recon, bits)
 
 
 def rel_l2(w_hat: np.ndarray, w: np.ndarray) -> float:

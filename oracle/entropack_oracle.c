@@ -1167,8 +1167,10 @@ double oracle_e4m3_to_f64(uint8_t b) {
 }
 
 /* FP8 comparator: per-row scale t = max|w| / 448 (FP32), w / t rounded to E4M3
-   (satfinite), reconstruction BF16(e4m3 * t).  8 + 32 / K bits per weight. */
-double oracle_fp8_row_roundtrip(const uint16_t *w, int64_t M, int64_t K, uint16_t *recon) {
+   (satfinite), reconstruction BF16(e4m3 * t).  8 + 32 / K bits per weight.
+   codes (M*K bytes) and scales (M floats) may be NULL. */
+double oracle_fp8_row_roundtrip(const uint16_t *w, int64_t M, int64_t K, uint16_t *recon, uint8_t *codes,
+                                float *scales) {
     for (int64_t r = 0; r < M; r++) {
         float s = 0.0f;
         for (int64_t c = 0; c < K; c++) {
@@ -1176,9 +1178,11 @@ double oracle_fp8_row_roundtrip(const uint16_t *w, int64_t M, int64_t K, uint16_
             if (a > s) s = a;
         }
         const float t = s / 448.0f;
+        if (scales) scales[r] = t;
         for (int64_t c = 0; c < K; c++) {
             const float x = t > 0.0f ? (float)oracle_bf16_to_f64(w[r * K + c]) / t : 0.0f;
             const uint8_t q = oracle_f32_to_e4m3_satfinite(x);
+            if (codes) codes[r * K + c] = q;
             recon[r * K + c] = oracle_f32_to_bf16((float)oracle_e4m3_to_f64(q) * t);
         }
     }

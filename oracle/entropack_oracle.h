@@ -95,7 +95,8 @@ void oracle_int4_levels(double cb[16]);
 double oracle_q4_roundtrip(const uint16_t *w, int64_t n, int64_t block, const double levels[16],
                            uint8_t *codes, float *scales, uint16_t *recon);
 double oracle_e4m3_to_f64(uint8_t b);
-double oracle_fp8_row_roundtrip(const uint16_t *w, int64_t M, int64_t K, uint16_t *recon);
+double oracle_fp8_row_roundtrip(const uint16_t *w, int64_t M, int64_t K, uint16_t *recon, uint8_t *codes,
+                                float *scales);
 
 /* fp64 reference GEMM: y[t, n] = sum_k x[t, k] * w[n, k] for rows t of x */
 void oracle_gemm_f64(const double *x, const double *w, double *y, int64_t T, int64_t N, int64_t K);

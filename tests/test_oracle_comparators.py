@@ -117,13 +117,16 @@ def test_e4m3_decoder_matches_torch():
 def test_fp8_row_roundtrip_matches_torch():
     w = synth.rows_outliers_bf16(22, 48, 256)
     w[5] = 0
-    recon, bits = oracle.fp8_row_roundtrip(w)
+    recon, bits, codes, scales = oracle.fp8_row_roundtrip(w, with_codes=True)
     wf = _f32(w)
     t = (np.abs(wf).max(axis=1) / np.float32(448.0)).astype(np.float32)
     x = np.where(t[:, None] > 0, wf / np.where(t > 0, t, 1)[:, None], 0).astype(np.float32)
-    q = torch.from_numpy(x).to(torch.float8_e4m3fn).float().numpy()
+    q8 = torch.from_numpy(x).to(torch.float8_e4m3fn)
+    q = q8.float().numpy()
     ref = _bf16_bits_of_f32(q * t[:, None])
     np.testing.assert_array_equal(recon, ref)
+    np.testing.assert_array_equal(scales.view(np.uint32), t.view(np.uint32))
+    np.testing.assert_array_equal(codes, q8.view(torch.uint8).numpy())
     assert bits == 8.0 + 32.0 / 256
 
 
