@@ -376,7 +376,8 @@ def bench_comparators(ep, synth, torch, np, device, stream, peaks, copies: int =
 
     W is 10240 x 3840 Student-t (nu = 5) BF16.  Relative L2 weight error
     ||W_hat - W|| / ||W|| (fp64, on the device) of EntroPack at a 4-bit target
-    and of NF4 / INT4 with block 64 and FP32 scales (4.5 bits per weight), all
+    and of NF4 / INT4 with block 64 and FP32 scales (4.5 bits per weight); of
+    per-row FP8 E4M3 (8 bits) against EntroPack at the same storage; all
     reconstructed by the library's kernels.  The NF4 reconstruction kernel is
     also timed on `copies` concatenated copies of the layer's codes (inputs
     and outputs far larger than L2) for its own HBM roofline.
@@ -426,6 +427,38 @@ def bench_comparators(ep, synth, torch, np, device, stream, peaks, copies: int =
                          "frac": alg / t / 1e9 / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": alg,
                          "kernel": "q4_decode_kernel"}})
         del big_codes, big_scales, big_out
+    # per-row FP8 E4M3 (8 bits per weight): quality on the layer, and its
+    # reconstruction kernel timed on the same concatenated size
+    codes, scales = ep.fp8_row_encode(w)
+    c_dev = torch.from_numpy(codes).to(device)
+    s_dev = torch.from_numpy(scales).to(device)
+    with torch.cuda.stream(stream):
+        y8 = ep.fp8_row_decode(c_dev, s_dev, stream=stream)
+    torch.cuda.synchronize(device)
+    out["fp8_row"] = {"bits_per_weight": 8.0 + 32.0 / K, "rel_l2": rel(y8)}
+    big_c = c_dev.repeat(copies, 1)
+    big_s = s_dev.repeat(copies)
+    big_y = torch.empty((copies * N, K), dtype=torch.bfloat16, device=device)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            ep.fp8_row_decode(big_c, big_s, out=big_y, stream=stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(10):
+            ep.fp8_row_decode(big_c, big_s, out=big_y, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize(device)
+    t = a.elapsed_time(b) / 10 / 1e3
+    alg = copies * n * (1.0 + 2.0) + copies * N * 4.0
+    out["fp8_row"].update({"decode_gparams_s": copies * n / t / 1e9, "decode_ms": t * 1e3,
+                           "roofline": {"bound": "hbm", "achieved": alg / t / 1e9, "peak": peaks["hbm_gbs"],
+                                        "unit": "GB/s", "frac": alg / t / 1e9 / peaks["hbm_gbs"],
+                                        "algorithmic_bytes_per_launch": alg, "kernel": "fp8_row_decode_kernel"}})
+    del big_c, big_s, big_y
+    # EntroPack at the FP8 comparator's storage (aimed 0.2 bit lower: metadata comes on top)
+    blob8 = ep.encode(w, out["fp8_row"]["bits_per_weight"] - 0.2)
+    y_e8, _ = ep.decode(ep.DeviceBlob(blob8, device=device), stream=stream)
+    out["entropack_at_fp8_storage"] = {"bits_per_weight": 8.0 * len(blob8) / n, "rel_l2": rel(y_e8)}
     out["rel_l2_entropack_over_nf4"] = out["entropack_4bpp"]["rel_l2"] / out["nf4_b64"]["rel_l2"]
     return out
 

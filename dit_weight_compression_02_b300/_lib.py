@@ -70,6 +70,8 @@ SIGNATURES = {
     "ep_q4_levels": (i32, [i32, P]),
     "ep_q4_encode": (i32, [P, i64, i64, P, P, P, i32]),
     "ep_q4_decode": (i32, [P, P, i64, i64, P, P, P]),
+    "ep_fp8_row_encode": (i32, [P, i64, i64, P, P, i32]),
+    "ep_fp8_row_decode": (i32, [P, P, i64, i64, P, P]),
 }
 
 for _name, (_res, _args) in SIGNATURES.items():

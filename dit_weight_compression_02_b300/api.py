@@ -401,6 +401,28 @@ def q4_decode(codes: torch.Tensor, scales: torch.Tensor, levels: np.ndarray, sha
     return y
 
 
+def fp8_row_encode(w_bits, n_threads: int = 0):
+    """ep_fp8_row_encode: per-row-scaled FP8 E4M3 comparator on the host -> (codes uint8, FP32 row scales)."""
+    w = bf16_bits(w_bits)
+    if w.ndim != 2:
+        raise ValueError("expected a 2-D weight matrix")
+    codes = np.zeros(w.shape, dtype=np.uint8)
+    scales = np.zeros(w.shape[0], dtype=np.float32)
+    check(lib.ep_fp8_row_encode(_ptr(w), w.shape[0], w.shape[1], _ptr(codes), _ptr(scales), int(n_threads)),
+          "ep_fp8_row_encode")
+    return codes, scales
+
+
+def fp8_row_decode(codes: torch.Tensor, scales: torch.Tensor, out: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """ep_fp8_row_decode: BF16 reconstruction of the FP8 comparator on the GPU."""
+    rows, cols = codes.shape
+    y = torch.empty((rows, cols), dtype=torch.bfloat16, device=codes.device) if out is None else out
+    check(lib.ep_fp8_row_decode(_ptr(codes), _ptr(scales), rows, cols, _ptr(y), _stream_handle(stream)),
+          "ep_fp8_row_decode")
+    return y
+
+
 # ------------------------------------------------------------ tensor-level API
 @dataclass
 class EntroPackLossyConfig:
@@ -533,5 +555,5 @@ __all__ = ["encode", "query", "actual_bpp", "DeviceBlob", "decode", "decode_into
            "linear_bf16", "compressed_linear", "LINEAR_DECODE_THEN_GEMM", "LINEAR_FUSED",
            "EntroPackLossyConfig", "TileANSConfig", "CompressedTensor", "compress", "decompress",
            "CompressedLinear", "EntroPackError", "CONTAINERS", "CONTAINER_DTYPES",
-           "q4_levels", "q4_encode", "q4_decode", "Q4Tensor", "Q4_KINDS",
+           "q4_levels", "q4_encode", "q4_decode", "Q4Tensor", "Q4_KINDS", "fp8_row_encode", "fp8_row_decode",
            "estimate_bpp", "allocate_bits", "compress_linears"]

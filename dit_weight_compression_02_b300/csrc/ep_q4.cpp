@@ -1,5 +1,5 @@
-// Host side of the fixed-width 4-bit comparators: codebook levels and the
-// block-absmax encoder.
+// Host side of the fixed-width comparators: the 4-bit codebook levels and
+// block-absmax encoder, and the per-row-scaled FP8 E4M3 encoder.
 //
 // These are the formats EntroPack is measured against ("EntroPack: Fast and
 // Accurate Entropy-Coded Weight Compression at Arbitrary Bitrates", Abstract:
@@ -91,6 +91,28 @@ bool encode_block(const uint16_t* w, int64_t lo, int64_t hi, const float* lv, ui
     return true;
 }
 
+// E4M3 (bias 7, 3 mantissa bits, subnormals below 2^-6, largest finite 448)
+// of a finite float, rounded to nearest even and saturated to +-448
+uint8_t e4m3_satfinite(float x) {
+    const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+    const float a = std::fabs(x);
+    if (a >= 448.0f) return sign | 0x7E;
+    if (a < 0.015625f) {  // below 2^-6: multiples of 2^-9, the byte is the multiple (8 = 2^-6)
+        const float q = std::nearbyint(a * 512.0f);
+        return sign | (uint8_t)q;
+    }
+    int e2 = 0;
+    std::frexp(a, &e2);  // a = f * 2^e2, f in [0.5, 1): the exponent of a is e2 - 1
+    const int e = e2 - 1;
+    float q = std::nearbyint(std::ldexp(a, 3 - e));  // 8 .. 16 in steps of 2^(e - 3)
+    int ee = e;
+    if (q >= 16.0f) {
+        q = 8.0f;
+        ee += 1;
+    }
+    return sign | (uint8_t)(((ee + 7) << 3) | ((int)q - 8));
+}
+
 }  // namespace
 
 extern "C" {
@@ -122,6 +144,43 @@ ep_status ep_q4_encode(const uint16_t* w, int64_t n, int64_t block, const float*
         for (int64_t b = b0; b < b1 && ok[(size_t)t]; ++b) {
             const int64_t lo = b * block, hi = lo + block < n ? lo + block : n;
             if (!encode_block(w, lo, hi, levels, codes, scales + b)) ok[(size_t)t] = 0;
+        }
+    };
+    std::vector<std::thread> pool;
+    for (int t = 1; t < threads; ++t) pool.emplace_back(work, t);
+    work(0);
+    for (auto& th : pool) th.join();
+    for (char c : ok)
+        if (!c) return EP_ERR_NONFINITE;
+    return EP_OK;
+}
+
+ep_status ep_fp8_row_encode(const uint16_t* w, int64_t rows, int64_t cols, uint8_t* codes, float* scales,
+                            int32_t n_threads) {
+    if (!w || !codes || !scales) return EP_ERR_INVALID_ARG;
+    if (rows <= 0 || cols <= 0 || cols % 8 || rows > (int64_t(1) << 40) || cols > (int64_t(1) << 40))
+        return EP_ERR_SHAPE;
+    int threads = n_threads > 0 ? n_threads : (int)std::thread::hardware_concurrency();
+    if (threads < 1) threads = 1;
+    if ((int64_t)threads > rows) threads = (int)rows;
+    std::vector<char> ok((size_t)threads, 1);
+    auto work = [&](int t) {
+        const int64_t r0 = rows * t / threads, r1 = rows * (t + 1) / threads;
+        for (int64_t r = r0; r < r1; ++r) {
+            const uint16_t* row = w + r * cols;
+            float s = 0.0f;
+            for (int64_t c = 0; c < cols; ++c) {
+                const float a = std::fabs(bf16_value(row[c]));
+                if (!std::isfinite(a)) {
+                    ok[(size_t)t] = 0;
+                    return;
+                }
+                if (a > s) s = a;
+            }
+            const float sc = s / 448.0f;
+            scales[r] = sc;
+            for (int64_t c = 0; c < cols; ++c)
+                codes[r * cols + c] = e4m3_satfinite(sc > 0.0f ? bf16_value(row[c]) / sc : 0.0f);
         }
     };
     std::vector<std::thread> pool;

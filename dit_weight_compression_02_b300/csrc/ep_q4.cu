@@ -1,4 +1,4 @@
-// GPU reconstruction of the fixed-width 4-bit comparators (NF4 / INT4):
+// GPU reconstruction of the fixed-width comparators.  NF4 / INT4:
 // out[i] = BF16(levels[code_i] * scale[i / block]), one FP32 product rounded
 // to nearest even.  The codes are packed two per byte, element 2j in the low
 // nibble of byte j.
@@ -8,6 +8,8 @@
 // scale, since block % 16 == 0) into 32 output bytes with two 16-byte stores;
 // a grid of whole waves strides over the groups.  A ragged tail (n % 16 != 0)
 // is finished element by element by the thread that owns the last group.
+// FP8 per row: out[r, c] = BF16(e4m3(code[r, c]) * scale[r]), 16 codes (one
+// 16-byte load) to two 16-byte stores per thread.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -64,7 +66,74 @@ __global__ void __launch_bounds__(kThreads) q4_decode_kernel(const uint2* __rest
     }
 }
 
+// E4M3 byte -> float, exact: normal (8 + m) 2^(e - 10), subnormal m 2^-9
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+    const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+    const float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;
+    return (b & 0x80u) ? -v : v;
+}
+
+// Per-row-scaled FP8 comparator: out[r, c] = BF16(e4m3(code[r, c]) * scale[r]).
+// One thread turns 16 codes (one 16-byte load) into two 16-byte stores; each
+// half of 8 codes lies in one row (cols % 8 == 0) and takes that row's scale.
+// With an odd number of 8-code groups the last one is done alone.
+__device__ __forceinline__ uint4 fp8_group(uint32_t lo, uint32_t hi, float s) {
+    uint32_t p[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const uint32_t word = h < 2 ? lo : hi;
+        const uint32_t b0 = (word >> (16 * (h & 1))) & 0xFFu, b1 = (word >> (16 * (h & 1) + 8)) & 0xFFu;
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(e4m3_value(b0) * s, e4m3_value(b1) * s);
+        p[h] = *reinterpret_cast<const uint32_t*>(&pr);
+    }
+    return make_uint4(p[0], p[1], p[2], p[3]);
+}
+
+__global__ void __launch_bounds__(kThreads) fp8_row_decode_kernel(const uint8_t* __restrict__ codes,
+                                                                  const float* __restrict__ scales, int64_t rows,
+                                                                  int64_t cols, uint4* __restrict__ out) {
+    const int64_t n8 = rows * cols / 8;  // 8-code groups
+    const int64_t per_row = cols / 8;
+    const int64_t n16 = n8 / 2;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    const uint4* c16 = reinterpret_cast<const uint4*>(codes);
+    for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < n16; g += stride) {
+        const uint4 c = __ldg(c16 + g);
+        const float s0 = __ldg(scales + (2 * g) / per_row);
+        const float s1 = __ldg(scales + (2 * g + 1) / per_row);
+        out[2 * g] = fp8_group(c.x, c.y, s0);
+        out[2 * g + 1] = fp8_group(c.z, c.w, s1);
+    }
+    if ((n8 & 1) && blockIdx.x == 0 && threadIdx.x == 0) {
+        const int64_t g8 = n8 - 1;
+        const uint2 c = __ldg(reinterpret_cast<const uint2*>(codes) + g8);
+        out[g8] = fp8_group(c.x, c.y, __ldg(scales + g8 / per_row));
+    }
+}
+
+int grid_for(int64_t work_items) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t per_wave = (int64_t)sms * (2048 / kThreads);
+    int64_t grid = (work_items + kThreads - 1) / kThreads;
+    if (grid > per_wave * 4) grid = per_wave * 4;
+    return (int)grid;
+}
+
 }  // namespace
+
+extern "C" ep_status ep_fp8_row_decode(const uint8_t* d_codes, const float* d_scales, int64_t rows, int64_t cols,
+                                       uint16_t* d_out, ep_stream_t stream) {
+    if (!d_codes || !d_scales || !d_out) return EP_ERR_INVALID_ARG;
+    if (rows <= 0 || cols <= 0 || cols % 8 || rows > (int64_t(1) << 40) || cols > (int64_t(1) << 40))
+        return EP_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(d_codes) & 15) || (reinterpret_cast<uintptr_t>(d_scales) & 3) ||
+        (reinterpret_cast<uintptr_t>(d_out) & 15))
+        return EP_ERR_INVALID_ARG;
+    fp8_row_decode_kernel<<<(unsigned)grid_for(rows * cols / 16 + 1), kThreads, 0, (cudaStream_t)stream>>>(
+        d_codes, d_scales, rows, cols, reinterpret_cast<uint4*>(d_out));
+    return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
 
 extern "C" ep_status ep_q4_decode(const uint8_t* d_codes, const float* d_scales, int64_t n, int64_t block,
                                   const float* levels, uint16_t* d_out, ep_stream_t stream) {

@@ -341,6 +341,23 @@ ep_status ep_q4_encode(const uint16_t *w, int64_t n, int64_t block, const float 
 ep_status ep_q4_decode(const uint8_t *d_codes, const float *d_scales, int64_t n, int64_t block, const float *levels,
                        uint16_t *d_out, ep_stream_t stream);
 
+/* Per-row-scaled FP8 comparator (8 + 32 / cols bits per weight): row r keeps
+ * t_r = max_c |w[r, c]| / 448 as FP32 and each weight the E4M3 byte of
+ * w / t_r (FP32 division; 0 when t_r = 0), rounded to nearest even and
+ * saturated to +-448; the reconstruction is BF16(e4m3 * t_r), one FP32
+ * product rounded to nearest even.
+ * Host: encode rows x cols BF16 weights (cols % 8 == 0) into codes (rows *
+ * cols bytes) and scales (rows floats), caller-owned host buffers.  Errors:
+ * EP_ERR_INVALID_ARG (NULL), EP_ERR_SHAPE, EP_ERR_NONFINITE. */
+ep_status ep_fp8_row_encode(const uint16_t *w, int64_t rows, int64_t cols, uint8_t *codes, float *scales,
+                            int32_t n_threads);
+/* Device: reconstruct into d_out (rows x cols BF16, 16-byte aligned) from
+ * d_codes (16-byte aligned) and d_scales; asynchronous on `stream`, allocates
+ * nothing.  Errors before launch: EP_ERR_INVALID_ARG, EP_ERR_SHAPE; EP_ERR_CUDA
+ * if the launch fails. */
+ep_status ep_fp8_row_decode(const uint8_t *d_codes, const float *d_scales, int64_t rows, int64_t cols,
+                            uint16_t *d_out, ep_stream_t stream);
+
 /* Synchronise `stream` and map the status word: 0 -> EP_OK, any bit -> EP_ERR_CORRUPT. */
 ep_status ep_sync_status(const uint32_t *d_status, ep_stream_t stream);
 

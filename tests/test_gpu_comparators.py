@@ -61,3 +61,27 @@ def test_q4_decode_into_offset_views(ep):
     assert (out.view(torch.int16).cpu().numpy().view(np.uint16) == recon).all()
     rest = torch.cat([buf[:8], buf[8 + w.size:]]).float()
     assert (rest == 7.0).all()
+
+
+@pytest.mark.parametrize("shape", [(48, 256), (5, 8), (100, 1000), (1024, 3840)])
+def test_fp8_row_decode_bit_exact(ep, shape):
+    w = synth.rows_outliers_bf16(shape[0] + 11, *shape)
+    w[0] = 0
+    codes, scales = ep.fp8_row_encode(w)
+    y = ep.fp8_row_decode(torch.from_numpy(codes).cuda(), torch.from_numpy(scales).cuda())
+    torch.cuda.synchronize()
+    recon, _ = oracle.fp8_row_roundtrip(w)
+    np.testing.assert_array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), recon)
+
+
+def test_fp8_row_decode_every_code(ep):
+    """All 254 finite E4M3 bytes under a few scales, against the oracle's decoder."""
+    b = np.array([v for v in range(256) if v not in (0x7F, 0xFF)] * 2, dtype=np.uint8)[:504].reshape(1, 504)
+    codes = np.repeat(b, 3, axis=0)
+    scales = np.array([1.0, 2.0 ** -20, 3.5], dtype=np.float32)
+    y = ep.fp8_row_decode(torch.from_numpy(codes).cuda(), torch.from_numpy(scales).cuda())
+    torch.cuda.synchronize()
+    got = y.float().cpu().numpy().astype(np.float64)
+    q = np.array([[oracle.e4m3_to_f64(v) for v in row] for row in codes])
+    ref = torch.from_numpy((q.astype(np.float32) * scales[:, None]).astype(np.float32)).to(torch.bfloat16)
+    np.testing.assert_array_equal(got, ref.float().numpy().astype(np.float64))

@@ -349,3 +349,24 @@ def test_streaming_decoder_uploads_and_decodes(ep):
             last = max(i for i in range(7) if i % 3 == k)
             assert (_np(bufs[k]) == oracle.decode(blobs[last])[0]).all()
     assert sd.upload_bytes == sum(len(b) for b in blobs)
+
+
+def test_streaming_decoder_reports_corruption(ep):
+    """Payload bytes that change in host memory after planning are caught by the device checks."""
+    ws = [synth.normal_bf16(95 + i, 256, 1024) for i in range(4)]
+    blobs = [oracle.encode(w, 4.0) for w in ws]
+    dbs = [ep.DeviceBlob(b) for b in blobs]
+    outs = [torch.empty((256, 1024), dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    sd = ep.StreamingDecoder(dbs, outs, chunk=2)
+    sd()
+    h = oracle.header(blobs[3])
+    host = dbs[3].host.numpy()
+    saved = host.copy()
+    for off in range(h["payload_off"] + 200, h["payload_off"] + 2000, 97):
+        host[off] ^= 0xFF
+    with pytest.raises(ep.EntroPackError) as e:
+        sd()
+    assert e.value.status == "EP_ERR_CORRUPT"
+    host[:] = saved
+    sd()  # clean again
+    assert (_np(outs[3]) == oracle.decode(blobs[3])[0]).all()

@@ -12,6 +12,7 @@ import os
 import re
 
 import numpy as np
+import torch
 import pytest
 
 import oracle
@@ -273,3 +274,41 @@ def test_allocation_errors():
         with pytest.raises(ep.EntroPackError) as e:
             ep.encode(layers[0], 4.0, j=j)
         assert e.value.status == "EP_ERR_INVALID_ARG"
+
+
+def _wide_range_bf16(seed, rows, cols):
+    """Weights spread over 2^-30 .. 2^0 with random signs: every E4M3 binade and the subnormals."""
+    rng = np.random.default_rng(seed)
+    v = np.exp2(rng.uniform(-30.0, 0.0, size=(rows, cols))) * rng.choice([-1.0, 1.0], size=(rows, cols))
+    return torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("shape", [(48, 256), (5, 8), (100, 1000), (33, 136)])
+def test_fp8_row_encoder_byte_identical(shape):
+    ep = _ep()
+    for w in (synth.rows_outliers_bf16(shape[0] + 7, *shape), _wide_range_bf16(shape[0], *shape)):
+        w[0] = 0
+        w[-1, :2] = 0x8000  # -0
+        codes, scales = ep.fp8_row_encode(w)
+        _, _, c_o, s_o = oracle.fp8_row_roundtrip(w, with_codes=True)
+        np.testing.assert_array_equal(codes, c_o)
+        np.testing.assert_array_equal(scales.view(np.uint32), s_o.view(np.uint32))
+
+
+def test_fp8_row_errors():
+    ep = _ep()
+    from dit_weight_compression_02_b300._lib import lib
+    w = synth.normal_bf16(41, 4, 64)
+    bad = w.copy()
+    bad[2, 7] = 0xFF80  # -inf
+    with pytest.raises(ep.EntroPackError) as e:
+        ep.fp8_row_encode(bad)
+    assert e.value.status == "EP_ERR_NONFINITE"
+    with pytest.raises(ep.EntroPackError) as e:
+        ep.fp8_row_encode(w[:, :60].copy())
+    assert e.value.status == "EP_ERR_SHAPE"
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.ep_fp8_row_decode(fake, fake, 4, 64, ctypes.c_void_p((1 << 20) + 8), None) == 1
+    assert lib.ep_fp8_row_decode(ctypes.c_void_p((1 << 20) + 8), fake, 4, 64, fake, None) == 1
+    assert lib.ep_fp8_row_decode(fake, fake, 4, 60, fake, None) == 2
+    assert lib.ep_fp8_row_decode(None, fake, 4, 64, fake, None) == 1
