@@ -23,6 +23,7 @@ struct Levels {
 };
 
 constexpr int kThreads = 256;
+static_assert(kThreads == 256, "the FP8 kernel tabulates one E4M3 value per thread");
 
 __global__ void __launch_bounds__(kThreads) q4_decode_kernel(const uint2* __restrict__ codes,
                                                              const float* __restrict__ scales, int64_t n,
@@ -74,16 +75,17 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
 }
 
 // Per-row-scaled FP8 comparator: out[r, c] = BF16(e4m3(code[r, c]) * scale[r]).
-// One thread turns 16 codes (one 16-byte load) into two 16-byte stores; each
+// The CTA first tabulates the 256 E4M3 values in shared memory (kThreads ==
+// 256).  One thread turns 16 codes (one 16-byte load) into two 16-byte stores; each
 // half of 8 codes lies in one row (cols % 8 == 0) and takes that row's scale.
 // With an odd number of 8-code groups the last one is done alone.
-__device__ __forceinline__ uint4 fp8_group(uint32_t lo, uint32_t hi, float s) {
+__device__ __forceinline__ uint4 fp8_group(const float* lut, uint32_t lo, uint32_t hi, float s) {
     uint32_t p[4];
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
         const uint32_t word = h < 2 ? lo : hi;
         const uint32_t b0 = (word >> (16 * (h & 1))) & 0xFFu, b1 = (word >> (16 * (h & 1) + 8)) & 0xFFu;
-        const __nv_bfloat162 pr = __floats2bfloat162_rn(e4m3_value(b0) * s, e4m3_value(b1) * s);
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(lut[b0] * s, lut[b1] * s);
         p[h] = *reinterpret_cast<const uint32_t*>(&pr);
     }
     return make_uint4(p[0], p[1], p[2], p[3]);
@@ -92,22 +94,29 @@ __device__ __forceinline__ uint4 fp8_group(uint32_t lo, uint32_t hi, float s) {
 __global__ void __launch_bounds__(kThreads) fp8_row_decode_kernel(const uint8_t* __restrict__ codes,
                                                                   const float* __restrict__ scales, int64_t rows,
                                                                   int64_t cols, uint4* __restrict__ out) {
+    __shared__ float lut[256];  // the value of every E4M3 byte
+    lut[threadIdx.x] = e4m3_value(threadIdx.x);
+    __syncthreads();
     const int64_t n8 = rows * cols / 8;  // 8-code groups
     const int64_t per_row = cols / 8;
     const int64_t n16 = n8 / 2;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     const uint4* c16 = reinterpret_cast<const uint4*>(codes);
+    const bool narrow = n8 < 0x7FFFFFFF;  // 32-bit row arithmetic suffices
     for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < n16; g += stride) {
         const uint4 c = __ldg(c16 + g);
-        const float s0 = __ldg(scales + (2 * g) / per_row);
-        const float s1 = __ldg(scales + (2 * g + 1) / per_row);
-        out[2 * g] = fp8_group(c.x, c.y, s0);
-        out[2 * g + 1] = fp8_group(c.z, c.w, s1);
+        // row of the first half by one division; the second half is in that row or the next
+        const int64_t r0 = narrow ? (int64_t)((uint32_t)(2 * g) / (uint32_t)per_row) : (2 * g) / per_row;
+        const int64_t r1 = r0 + ((2 * g + 1) >= (r0 + 1) * per_row ? 1 : 0);
+        const float s0 = __ldg(scales + r0);
+        const float s1 = __ldg(scales + r1);
+        out[2 * g] = fp8_group(lut, c.x, c.y, s0);
+        out[2 * g + 1] = fp8_group(lut, c.z, c.w, s1);
     }
     if ((n8 & 1) && blockIdx.x == 0 && threadIdx.x == 0) {
         const int64_t g8 = n8 - 1;
         const uint2 c = __ldg(reinterpret_cast<const uint2*>(codes) + g8);
-        out[g8] = fp8_group(c.x, c.y, __ldg(scales + g8 / per_row));
+        out[g8] = fp8_group(lut, c.x, c.y, __ldg(scales + g8 / per_row));
     }
 }
 
