@@ -312,3 +312,11 @@ def test_fp8_row_errors():
     assert lib.ep_fp8_row_decode(ctypes.c_void_p((1 << 20) + 8), fake, 4, 64, fake, None) == 1
     assert lib.ep_fp8_row_decode(fake, fake, 4, 60, fake, None) == 2
     assert lib.ep_fp8_row_decode(None, fake, 4, 64, fake, None) == 1
+
+
+def test_allocation_thread_count_does_not_change_the_plan():
+    ep = _ep()
+    layers = _alloc_layers()
+    ref = ep.allocate_bits(layers, 3.0, [1.0, 2.0, 0.5], n_threads=1)
+    for t in (2, 5):
+        assert ep.allocate_bits(layers, 3.0, [1.0, 2.0, 0.5], n_threads=t) == ref
