@@ -67,6 +67,10 @@ SIGNATURES = {
     "ep_encode_at": (i32, [P, i64, i64, ctypes.POINTER(EpParams), i32, ctypes.POINTER(P), ctypes.POINTER(sz)]),
     "ep_estimate_bpp": (i32, [P, i64, i64, f32, i32, i32, ctypes.POINTER(f64), ctypes.POINTER(i32)]),
     "ep_allocate_bits": (i32, [ctypes.POINTER(EpLayerRef), i64, f32, f32, i32, P, P, ctypes.POINTER(i32)]),
+    "ep_stream_open": (i32, [P, sz, ctypes.POINTER(P)]),
+    "ep_stream_close": (None, [P]),
+    "ep_decode_h": (i32, [P, P, P, P, P, P]),
+    "ep_compressed_linear_h": (i32, [P, P, P, i64, P, P, i32, P, sz, P, P]),
     "ep_q4_levels": (i32, [i32, P]),
     "ep_q4_encode": (i32, [P, i64, i64, P, P, P, i32]),
     "ep_q4_decode": (i32, [P, P, i64, i64, P, P, P]),

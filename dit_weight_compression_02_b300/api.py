@@ -165,6 +165,19 @@ class DeviceBlob:
         self.device = torch.empty(self.host.numel(), dtype=torch.uint8, device=device)
         self.device.copy_(self.host, non_blocking=False)
         self.nbytes = self.host.numel()
+        # the stream validated once (ep_stream_open): hot paths launch from it
+        # without parsing the host copy again
+        self.handle = ctypes.c_void_p(0)
+        check(lib.ep_stream_open(_ptr(self.host), self.nbytes, ctypes.byref(self.handle)), "ep_stream_open")
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value:
+            try:
+                lib.ep_stream_close(h)
+            except Exception:  # interpreter shutdown
+                pass
+            self.handle = ctypes.c_void_p(0)
 
     @property
     def shape(self):
@@ -179,8 +192,15 @@ class DeviceBlob:
 
 
 def decode_into(db: DeviceBlob, out: torch.Tensor, row_scale: torch.Tensor | None, status: torch.Tensor,
-                stream=None, sym_out: torch.Tensor | None = None) -> None:
-    """Enqueue ep_decode (or ep_decode_symbols) on `stream`; no synchronisation."""
+                stream=None, sym_out: torch.Tensor | None = None, validated: bool = False) -> None:
+    """Enqueue ep_decode (or ep_decode_symbols) on `stream`; no synchronisation.
+
+    validated=True launches from the stream handle (ep_decode_h): the host copy
+    was validated when the DeviceBlob was made and is not parsed again."""
+    if validated and sym_out is None:
+        check(lib.ep_decode_h(db.handle, _ptr(db.device), _ptr(out), _ptr(row_scale), _ptr(status),
+                              _stream_handle(stream)), "ep_decode_h")
+        return
     args = (_ptr(db.host), _ptr(db.device), db.nbytes, _ptr(out), _ptr(row_scale))
     if sym_out is None:
         check(lib.ep_decode(*args, _ptr(status), _stream_handle(stream)), "ep_decode")
@@ -345,9 +365,10 @@ def compressed_linear(db: DeviceBlob, x: torch.Tensor, mode: int = LINEAR_DECODE
         workspace = torch.empty(rows * cols, dtype=torch.bfloat16, device=x.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = torch.zeros(1, dtype=torch.int32, device=x.device) if status is None else status
-    check(lib.ep_compressed_linear(_ptr(db.host), _ptr(db.device), db.nbytes, _ptr(x), x.shape[0], _ptr(y),
-                                   _ptr(bias), int(mode), _ptr(workspace), ws_bytes, _ptr(st), _stream_handle(stream)),
-          "ep_compressed_linear")
+    # launched from the stream handle: the host copy was validated when the DeviceBlob was made
+    check(lib.ep_compressed_linear_h(db.handle, _ptr(db.device), _ptr(x), x.shape[0], _ptr(y), _ptr(bias),
+                                     int(mode), _ptr(workspace), ws_bytes, _ptr(st), _stream_handle(stream)),
+          "ep_compressed_linear_h")
     if status is None:
         sync_status(st, stream)
     return y
@@ -505,7 +526,7 @@ class CompressedLinear(torch.nn.Module):
         if self._ws is None:
             self._ws = torch.empty(self.ct.shape, dtype=torch.bfloat16, device=dev)
             self._status = torch.zeros(1, dtype=torch.int32, device=dev)
-        decode_into(self.ct.blob, self._ws, None, self._status, stream)
+        decode_into(self.ct.blob, self._ws, None, self._status, stream, validated=True)
         return self._ws
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:

@@ -67,3 +67,8 @@ inline size_t container_bytes(int container) {
 }
 
 }  // namespace ep
+
+// the opaque handle of the C ABI: a parsed, validated stream layout
+struct ep_stream_handle {
+    ep::Layout L;
+};

@@ -305,6 +305,26 @@ ep_status check_gemm_args(const void* d_x, const void* d_w, const void* d_y, con
 }
 
 }  // namespace
+
+// CompressedLinear on a stream already parsed and validated into L
+ep_status compressed_linear_parsed(const Layout& L, const void* d_blob, const uint16_t* d_x, int64_t tokens,
+                                   uint16_t* d_y, const uint16_t* d_bias, int32_t mode, void* d_ws, size_t ws_bytes,
+                                   uint32_t* d_status, ep_stream_t stream) {
+    ep_status st;
+    if (L.mode != EP_MODE_LOSSY_E8 || L.container != EP_C_BF16) return EP_ERR_UNSUPPORTED;
+    if (mode != EP_LINEAR_DECODE_THEN_GEMM) return EP_ERR_UNSUPPORTED;
+    const size_t need = (size_t)L.rows * (size_t)L.cols * 2u;
+    if (!d_ws || ws_bytes < need) return EP_ERR_INVALID_ARG;
+    st = check_gemm_args(d_x, d_ws, d_y, d_bias, tokens, L.rows, L.cols, d_status);
+    if (st != EP_OK) return st;
+    // the decode zeroes the status word and writes W into the workspace; the
+    // GEMM (same stream) reads it back, mostly from L2
+    st = decode_parsed(L, d_blob, d_ws, nullptr, d_status, stream);
+    if (st != EP_OK) return st;
+    return gemm_launch(d_x, static_cast<const uint16_t*>(d_ws), d_y, d_bias, tokens, L.rows, L.cols, d_status,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // namespace ep
 
 extern "C" {
@@ -326,18 +346,15 @@ ep_status ep_compressed_linear(const uint8_t* h_blob, const void* d_blob, size_t
     thread_local Layout L;  // parsed and validated once per call
     ep_status st = parse_and_validate(h_blob, bytes, &L);
     if (st != EP_OK) return st;
-    if (L.mode != EP_MODE_LOSSY_E8 || L.container != EP_C_BF16) return EP_ERR_UNSUPPORTED;
-    if (mode != EP_LINEAR_DECODE_THEN_GEMM) return EP_ERR_UNSUPPORTED;
-    const size_t need = (size_t)L.rows * (size_t)L.cols * 2u;
-    if (!d_ws || ws_bytes < need) return EP_ERR_INVALID_ARG;
-    st = check_gemm_args(d_x, d_ws, d_y, d_bias, tokens, L.rows, L.cols, d_status);
-    if (st != EP_OK) return st;
-    // the decode zeroes the status word and writes W into the workspace; the
-    // GEMM (same stream) reads it back, mostly from L2
-    st = decode_parsed(L, d_blob, d_ws, nullptr, d_status, stream);
-    if (st != EP_OK) return st;
-    return gemm_launch(d_x, static_cast<const uint16_t*>(d_ws), d_y, d_bias, tokens, L.rows, L.cols, d_status,
-                       reinterpret_cast<cudaStream_t>(stream));
+    return compressed_linear_parsed(L, d_blob, d_x, tokens, d_y, d_bias, mode, d_ws, ws_bytes, d_status, stream);
+}
+
+ep_status ep_compressed_linear_h(const ep_stream_handle* h, const void* d_blob, const uint16_t* d_x, int64_t tokens,
+                                 uint16_t* d_y, const uint16_t* d_bias, int32_t mode, void* d_ws, size_t ws_bytes,
+                                 uint32_t* d_status, ep_stream_t stream) {
+    if (!h || !d_blob || !d_status) return EP_ERR_INVALID_ARG;
+    return ep::compressed_linear_parsed(h->L, d_blob, d_x, tokens, d_y, d_bias, mode, d_ws, ws_bytes, d_status,
+                                        stream);
 }
 
 }  // extern "C"

@@ -191,6 +191,28 @@ ep_status ep_decode_symbols(const uint8_t *h_blob, const void *d_blob, size_t by
                             float *d_row_scale_out, uint8_t *d_sym_out, uint32_t *d_status, ep_stream_t stream);
 
 /*
+ * Validated stream handles.  ep_decode and ep_compressed_linear parse and
+ * validate the host copy on every call (tens of microseconds per layer).
+ * A handle keeps the parsed layout so that a stream decoded many times (a
+ * CompressedLinear in a denoising loop) is validated once:
+ *   ep_stream_open   parse and fully validate h_blob; *out is owned by the
+ *                    caller (release with ep_stream_close).  Errors as
+ *                    ep_query, plus EP_ERR_NOMEM.  The handle keeps no
+ *                    pointer to h_blob.
+ *   ep_decode_h      ep_decode of the stream the handle describes; d_blob
+ *                    must hold its bytes on the device (16-byte aligned).
+ *                    The kernels re-check every tile against the stream
+ *                    size, so different device bytes can only raise
+ *                    EP_ERR_CORRUPT in the status word.
+ *   ep_compressed_linear_h   ep_compressed_linear likewise.
+ */
+typedef struct ep_stream_handle ep_stream_handle;
+ep_status ep_stream_open(const uint8_t *h_blob, size_t bytes, ep_stream_handle **out);
+void ep_stream_close(ep_stream_handle *h);
+ep_status ep_decode_h(const ep_stream_handle *h, const void *d_blob, void *d_out, float *d_row_scale_out,
+                      uint32_t *d_status, ep_stream_t stream);
+
+/*
  * Batched decode: many streams (e.g. every linear layer of a model) in one
  * persistent launch.  All items must share mode and container.  Work is cut
  * into units of 32 groups of 8 tiles (256 tiles) of one item; CTAs (one per
@@ -271,6 +293,9 @@ ep_status ep_linear_bf16(const uint16_t *d_x, const uint16_t *d_w, uint16_t *d_y
 ep_status ep_compressed_linear(const uint8_t *h_blob, const void *d_blob, size_t bytes, const uint16_t *d_x,
                                int64_t tokens, uint16_t *d_y, const uint16_t *d_bias, int32_t mode, void *d_ws,
                                size_t ws_bytes, uint32_t *d_status, ep_stream_t stream);
+ep_status ep_compressed_linear_h(const ep_stream_handle *h, const void *d_blob, const uint16_t *d_x, int64_t tokens,
+                                 uint16_t *d_y, const uint16_t *d_bias, int32_t mode, void *d_ws, size_t ws_bytes,
+                                 uint32_t *d_status, ep_stream_t stream);
 
 /*
  * Allocation-free variant of ep_batch_prepare + ep_batch_decode.  The pages

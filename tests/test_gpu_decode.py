@@ -370,3 +370,24 @@ def test_streaming_decoder_reports_corruption(ep):
     host[:] = saved
     sd()  # clean again
     assert (_np(outs[3]) == oracle.decode(blobs[3])[0]).all()
+
+
+def test_decode_from_validated_handle(ep):
+    """ep_decode_h (the stream parsed once) matches the oracle, and device-side checks still fire."""
+    w = synth.rows_outliers_bf16(97, 300, 1000)
+    blob = oracle.encode(w, 3.5)
+    db = ep.DeviceBlob(blob)
+    out = db.alloc_out()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        ep.decode_into(db, out, None, status, validated=True)
+        ep.sync_status(status)
+        assert (_np(out) == oracle.decode(blob)[0]).all()
+    h = oracle.header(blob)
+    b = bytearray(blob)
+    for off in range(h["payload_off"] + 200, h["payload_off"] + 2000, 97):
+        b[off] ^= 0xFF
+    db.device.copy_(torch.from_numpy(np.frombuffer(bytes(b), dtype=np.uint8).copy()).cuda())
+    ep.decode_into(db, out, None, status, validated=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 0x1

@@ -320,3 +320,28 @@ def test_allocation_thread_count_does_not_change_the_plan():
     ref = ep.allocate_bits(layers, 3.0, [1.0, 2.0, 0.5], n_threads=1)
     for t in (2, 5):
         assert ep.allocate_bits(layers, 3.0, [1.0, 2.0, 0.5], n_threads=t) == ref
+
+
+def test_stream_handles_validate_once():
+    """ep_stream_open parses and validates like ep_query; the handle entry points check their arguments."""
+    ep = _ep()
+    from dit_weight_compression_02_b300._lib import lib
+    blob = ep.encode(synth.normal_bf16(42, 64, 256), 4.0)
+    host = np.frombuffer(blob, dtype=np.uint8)
+    h = ctypes.c_void_p(0)
+    assert lib.ep_stream_open(host.ctypes.data, len(blob), ctypes.byref(h)) == 0 and h.value
+    fake = ctypes.c_void_p(1 << 20)
+    status = ctypes.c_void_p(1 << 21)
+    assert lib.ep_decode_h(h, ctypes.c_void_p((1 << 20) + 8), fake, None, status, None) == 1  # misaligned
+    assert lib.ep_decode_h(None, fake, fake, None, status, None) == 1
+    assert lib.ep_decode_h(h, fake, fake, None, None, None) == 1
+    assert lib.ep_compressed_linear_h(None, fake, fake, 16, fake, None, 0, fake, 1 << 30, status, None) == 1
+    assert lib.ep_compressed_linear_h(h, fake, fake, 16, fake, None, 1, fake, 1 << 30, status, None) == 5  # fused
+    assert lib.ep_compressed_linear_h(h, fake, fake, 16, fake, None, 0, fake, 10, status, None) == 1  # workspace
+    lib.ep_stream_close(h)
+    lib.ep_stream_close(None)
+    bad = np.frombuffer(_flip(blob, 0), dtype=np.uint8)
+    h2 = ctypes.c_void_p(0)
+    assert lib.ep_stream_open(bad.ctypes.data, len(blob), ctypes.byref(h2)) == 4 and not h2.value
+    assert lib.ep_stream_open(host.ctypes.data, len(blob) - 16, ctypes.byref(h2)) == 4
+    assert lib.ep_stream_open(None, len(blob), ctypes.byref(h2)) == 1
