@@ -860,28 +860,6 @@ ep_status ep_decode_symbols(const uint8_t* h_blob, const void* d_blob, size_t by
                            reinterpret_cast<cudaStream_t>(stream));
 }
 
-ep_status ep_stream_open(const uint8_t* h_blob, size_t bytes, ep_stream_handle** out) {
-    if (!h_blob || !out) return EP_ERR_INVALID_ARG;
-    *out = nullptr;
-    ep_stream_handle* h = new (std::nothrow) ep_stream_handle;
-    if (!h) return EP_ERR_NOMEM;
-    const ep_status st = ep::parse_and_validate(h_blob, bytes, &h->L);
-    if (st != EP_OK) {
-        delete h;
-        return st;
-    }
-    *out = h;
-    return EP_OK;
-}
-
-void ep_stream_close(ep_stream_handle* h) { delete h; }
-
-ep_status ep_decode_h(const ep_stream_handle* h, const void* d_blob, void* d_out, float* d_row_scale_out,
-                      uint32_t* d_status, ep_stream_t stream) {
-    if (!h) return EP_ERR_INVALID_ARG;
-    return ep::decode_parsed(h->L, d_blob, d_out, d_row_scale_out, d_status, stream);
-}
-
 size_t ep_batch_workspace_bytes(int64_t n_items) {
     if (n_items <= 0) return 0;
     size_t a, b, c;

@@ -152,4 +152,27 @@ ep_status ep_actual_bpp(const uint8_t* blob, size_t bytes, double* bpp) {
     return st;
 }
 
+// Validated stream handles: the layout parsed once, launched many times.
+ep_status ep_stream_open(const uint8_t* h_blob, size_t bytes, ep_stream_handle** out) {
+    if (!h_blob || !out) return EP_ERR_INVALID_ARG;
+    *out = nullptr;
+    ep_stream_handle* h = new (std::nothrow) ep_stream_handle;
+    if (!h) return EP_ERR_NOMEM;
+    const ep_status st = ep::parse_and_validate(h_blob, bytes, &h->L);
+    if (st != EP_OK) {
+        delete h;
+        return st;
+    }
+    *out = h;
+    return EP_OK;
+}
+
+void ep_stream_close(ep_stream_handle* h) { delete h; }
+
+ep_status ep_decode_h(const ep_stream_handle* h, const void* d_blob, void* d_out, float* d_row_scale_out,
+                      uint32_t* d_status, ep_stream_t stream) {
+    if (!h) return EP_ERR_INVALID_ARG;
+    return ep::decode_parsed(h->L, d_blob, d_out, d_row_scale_out, d_status, stream);
+}
+
 }  // extern "C"
