@@ -345,3 +345,16 @@ def test_stream_handles_validate_once():
     assert lib.ep_stream_open(bad.ctypes.data, len(blob), ctypes.byref(h2)) == 4 and not h2.value
     assert lib.ep_stream_open(host.ctypes.data, len(blob) - 16, ctypes.byref(h2)) == 4
     assert lib.ep_stream_open(None, len(blob), ctypes.byref(h2)) == 1
+
+
+def test_allocation_identical_to_oracle_random_cases():
+    """Seeded random sensitivities (FP32-exact) and budgets: library and oracle give the same plan."""
+    ep = _ep()
+    rng = np.random.default_rng(2024)
+    layers = _alloc_layers()
+    for _ in range(8):
+        sens = [float(np.float32(v)) for v in np.exp2(rng.uniform(-3.0, 3.0, size=3))]
+        avg = float(np.float32(rng.uniform(1.0, 7.0)))
+        r_lib = ep.allocate_bits(layers, avg, sens)
+        r_orc = oracle.allocate_bits(layers, avg, sens)
+        assert (r_lib["t"], r_lib["j"]) == (r_orc["t"], r_orc["j"]), (sens, avg)
