@@ -94,9 +94,9 @@ double oracle_bf16_to_f64(uint16_t b) {
 
 /* block b of a tile -> (row in tile, first column in tile) */
 static void block_place(int b, int *row, int *col) {
-    int slab = b / 64, rem = b % 64;
-    *row = rem / 2;
-    *col = 16 * slab + 8 * (rem % 2);
+    int slab = b / 128, rem = b % 128;
+    *row = rem / 4;
+    *col = 32 * slab + 8 * (rem % 4);
 }
 
 /* ------------------------------------------------- row scale and grid (§4.1) */
