@@ -10,9 +10,10 @@
 // stream's slot tables in shared memory (one u32 per 12-bit slot), which
 // leaves most of the SM's 256 KB L1 to cache the 1024 lane word streams
 // (each lane reads its 16-bit words in order, 16 words per 32-byte sector).
-// A lane decodes its 128 blocks of 8 coordinates in the format's order; lanes
-// 2h and 2h+1 of a tile write the two halves of one 32-byte row segment, so
-// every warp-wide 128-bit store covers whole sectors.  Escapes (values beyond
+// A lane decodes its 128 blocks of 8 coordinates in the format's order; the
+// four lanes of a tile write the four quarters of one 64-byte row segment, so
+// every warp-wide 128-bit store covers whole 64-byte units of HBM (a half
+// written unit costs a read-modify-write in the memory system).  Escapes (values beyond
 // the direct byte range) are rare: the fast path is branch-free and a
 // warp-uniform test sends a block with any escape through the slow path.
 //
@@ -39,6 +40,8 @@ namespace ep {
 namespace {
 
 constexpr int kThreads = 1024;
+constexpr int kSlabs = 4;        // K-slabs of a tile
+constexpr int kSlabCols = 32;    // columns of a K-slab
 constexpr int kTilesPerWarp = 8;
 constexpr int kSlots = 4096;
 constexpr uint32_t kMagicLo = 0x44C00000u;  // 1536.0f: bits 12..19 carry u, worth u/2
@@ -295,11 +298,11 @@ template <int KIND>
 struct LaneTile {
     bool active;
     const uint8_t* tb;  // tile payload (lossless: raw bytes first)
-    int64_t base;       // output element offset of the lane's block (slab 0, m2 0)
-    int32_t rows_left;  // true rows from the lane's first row on, capped at 32 (blocks with 2 m2 >= rows_left are padding)
-    int64_t col0;       // the lane's first column in slab 0 (blocks at col0 + 16 slab >= cols are padding)
-    const float* gr;    // row steps of the lane's rows: gr[2 m2]
-    const float* mr;    // FP8/INT8 multipliers: mr[2 m2]
+    int64_t base;       // output element offset of the lane's block in slab 0, tile row 0
+    int32_t rows_left;  // true rows of the tile, capped at 32 (blocks in tile rows >= rows_left are padding)
+    int64_t col0;       // the lane's first column in slab 0 (blocks at col0 + 32 slab >= cols are padding)
+    const float* gr;    // row steps of the tile's rows: gr[row]
+    const float* mr;    // FP8/INT8 multipliers: mr[row]
     float gnext;        // row step of the next block (prefetched one block ahead)
 
     // validate the tile, find the lane's words and start the lane
@@ -345,11 +348,11 @@ struct LaneTile {
         const int64_t t = active ? tile : 0;
         const int64_t tr0 = (t / a.tiles_per_row) * kTileRows;
         const int64_t tc0 = (t % a.tiles_per_row) * kTileCols;
-        // this lane's block of step j sits at tile row 2 (j % 16) + l / 2 and
-        // tile column 16 (j / 16) + 8 (l % 2)
-        const int64_t row0 = tr0 + (l >> 1);
+        // this lane's block of step j sits at tile row j % 32 and tile column
+        // 32 (j / 32) + 8 l: the tile's four lanes write one 64-byte row segment
+        const int64_t row0 = tr0;
         rows_left = (int32_t)min(a.rows - row0, (int64_t)kTileRows);
-        col0 = tc0 + 8 * (l & 1);
+        col0 = tc0 + 8 * l;
         base = row0 * a.cols + col0;
         gr = a.g + row0;
         mr = a.m + row0;
@@ -366,7 +369,7 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
     // descriptors live in global memory, which the output stores could alias
     void* const outp = a.out;
     uint8_t* const symp = a.sym_out;
-    const int64_t step = 2 * a.cols;
+    const int64_t step = a.cols;
     const int l = threadIdx.x & 3;
     Lane ln[NL];
     LaneTile<KIND> T[NL];
@@ -377,17 +380,17 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
         esc_bad[i] = false;
     }
 
-    for (int slab = 0; slab < 8; slab++) {
+    for (int slab = 0; slab < kSlabs; slab++) {
         int64_t eoff[NL];
         bool col_in[NL];  // the slab's block lies inside the true columns
 #pragma unroll
         for (int i = 0; i < NL; i++) {
-            eoff[i] = T[i].base + 16 * slab;
-            col_in[i] = T[i].active && (!RAGGED || T[i].col0 + 16 * slab < a.cols);
+            eoff[i] = T[i].base + kSlabCols * slab;
+            col_in[i] = T[i].active && (!RAGGED || T[i].col0 + kSlabCols * slab < a.cols);
         }
 #pragma unroll 2
-        for (int m2 = 0; m2 < 16; m2++) {
-            const int j = slab * 16 + m2;
+        for (int row = 0; row < kTileRows; row++) {
+            const int j = slab * kTileRows + row;
             top_up<NL>(ln);
             if constexpr (is_lossless(KIND)) {
                 uint32_t e[NL][8];
@@ -397,7 +400,7 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
                     for (int i = 0; i < NL; i++) e[i][k] = ln[i].sym(tab);
 #pragma unroll
                 for (int i = 0; i < NL; i++) {
-                    const bool st = col_in[i] && (!RAGGED || 2 * m2 < T[i].rows_left);
+                    const bool st = col_in[i] && (!RAGGED || row < T[i].rows_left);
                     // raw bytes of block 4 j + l start at raw_per_elem * 8 * (4 j + l)
                     const uint8_t* rp = T[i].tb + raw_per_elem(KIND) * 8 * (4 * j + l);
                     if constexpr (KIND == K_LOSSLESS) {
@@ -461,8 +464,8 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
 #pragma unroll
             for (int i = 0; i < NL; i++) {
                 mult[i] = T[i].gnext;  // prefetched one block ahead (the L1 beside the rings is small)
-                T[i].gnext = (T[i].active && j + 1 < kBlocksPerLane) ? __ldg(T[i].gr + 2 * ((m2 + 1) & 15)) : 0.f;
-                if (KIND == K_FP8 || KIND == K_INT8) mult[i] = T[i].active ? __ldg(T[i].mr + 2 * m2) : 0.f;
+                T[i].gnext = (T[i].active && j + 1 < kBlocksPerLane) ? __ldg(T[i].gr + ((row + 1) & 31)) : 0.f;
+                if (KIND == K_FP8 || KIND == K_INT8) mult[i] = T[i].active ? __ldg(T[i].mr + row) : 0.f;
             }
             uint32_t e[NL][8];
             const uint32_t* t1[NL];
@@ -525,7 +528,7 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
 #pragma unroll
                     for (int k = 0; k < 8; k++) y[k] = fmaf(__uint_as_float(F[k]), mult[i], cst);
                 }
-                if (col_in[i] && (!RAGGED || 2 * m2 < T[i].rows_left)) {
+                if (col_in[i] && (!RAGGED || row < T[i].rows_left)) {
                     store_block<KIND>(outp, eoff[i], y);
                     if (DUMP) {
                         uint32_t u[8];

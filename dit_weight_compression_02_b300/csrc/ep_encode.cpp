@@ -213,9 +213,9 @@ bool rans_lane(const uint8_t* sym, const uint8_t* ctx, int n, const SymTable& T,
 
 // tile block b -> (row in tile, first column in tile)
 inline void tile_block(int b, int* r, int* c) {
-    const int slab = b >> 6, rem = b & 63;
-    *r = rem >> 1;
-    *c = 16 * slab + 8 * (rem & 1);
+    const int slab = b >> 7, rem = b & 127;
+    *r = rem >> 2;
+    *c = 32 * slab + 8 * (rem & 3);
 }
 
 inline uint64_t up16(uint64_t v) { return (v + 15) & ~(uint64_t)15; }
