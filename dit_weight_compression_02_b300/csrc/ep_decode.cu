@@ -5,17 +5,19 @@
 // reconstruction on the GPU"; containers BF16, FP16, FP8, INT8).
 //
 // Work decomposition.  A tile (32 x 128 weights) carries 4 independent rANS
-// lanes; one thread owns one lane, so one warp decodes a group of 8 tiles.
-// A CTA is 1024 threads, one per SM: its 32 warps share one copy of the
-// stream's slot tables in shared memory (one u32 per 12-bit slot), which
-// leaves most of the SM's 256 KB L1 to cache the 1024 lane word streams
-// (each lane reads its 16-bit words in order, 16 words per 32-byte sector).
+// lanes; thread (tig, l) of a warp runs lane l of tile tig, so one warp
+// decodes a group of 8 tiles, and a thread running NL lanes interleaves NL
+// groups.  One persistent CTA per SM: 1024 threads of one lane each, or 640
+// threads of two lanes each (1280 lanes), share one copy of the stream's slot
+// tables in shared memory (one u32 per 12-bit slot); each lane stages its
+// 16-bit words in a 64-byte shared-memory ring.
 // A lane decodes its 128 blocks of 8 coordinates in the format's order; the
 // four lanes of a tile write the four quarters of one 64-byte row segment, so
 // every warp-wide 128-bit store covers whole 64-byte units of HBM (a half
-// written unit costs a read-modify-write in the memory system).  Escapes (values beyond
-// the direct byte range) are rare: the fast path is branch-free and a
-// warp-uniform test sends a block with any escape through the slow path.
+// written unit costs a read-modify-write in the memory system).  Escapes
+// (values beyond the direct byte range) are rare: the fast path is
+// branch-free and a warp-uniform test sends a block with any escape through
+// the slow path, which reads the escape payload's words from global memory.
 //
 // Slot entry: f << 20 | u << 12 | (slot - cum_u), with f the 12-bit frequency
 // and u the symbol byte.  One LDS, one shift, one AND and one IMAD advance
@@ -29,6 +31,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -39,7 +42,10 @@
 namespace ep {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 1024;   // threads of a one-lane CTA
+// threads of a CTA whose threads run NL lanes each: 1024 x 1 or 640 x 2 (two
+// lanes per thread at 20 warps leave the compiler room to interleave them)
+__host__ __device__ constexpr int cta_threads(int nl) { return nl == 1 ? kThreads : 640; }
 constexpr int kSlabs = 4;        // K-slabs of a tile
 constexpr int kSlabCols = 32;    // columns of a K-slab
 constexpr int kTilesPerWarp = 8;
@@ -133,13 +139,14 @@ __device__ void build_tables(const DecodeArgs& a, uint32_t* tab, uint32_t* fr, u
 
 // ---------------------------------------------------------------- rANS lane
 // State x in [2^16, 2^32) before every symbol.  A lane's 16-bit words are
-// staged in a private 128-byte ring in shared memory (8 chunks of 16 bytes,
-// chunk c of the payload in slot c % 8), filled by cp.async at block
-// boundaries (top_up).  Every symbol reads the word at the lane's position
+// staged in a private 64-byte ring in shared memory (4 chunks of 16 bytes,
+// chunk c of the payload in slot c % 4), filled by cp.async before every
+// pair of blocks (top_up).  Every symbol reads the word at the lane's position
 // together with its slot-table entry, so the refill never waits on a load
 // issued for an earlier symbol: the warp's register scoreboard would
 // otherwise stall all 32 lanes on whichever lane refilled last.
-constexpr uint32_t kRingChunks = 8;
+constexpr uint32_t kRingChunks = 4;
+constexpr uint32_t kRingBytesPerLane = kRingChunks * 16;
 
 extern __shared__ __align__(128) uint32_t g_smem[];  // the decode CTA's dynamic shared memory
 
@@ -147,13 +154,13 @@ struct Lane {
     uint32_t x, next;
     uint32_t a, aend;       // payload byte offsets: next word, one past the lane's last word
     uint32_t issued, clast;  // next chunk to stage, last chunk of the lane (chunk = 16 bytes)
-    uint32_t roff;           // byte offset of the lane's 128-byte ring in g_smem (a multiple of 128)
+    uint32_t roff;           // byte offset of the lane's 64-byte ring in g_smem (a multiple of 64)
     uint32_t ring;           // shared-window address of the same ring (for cp.async)
     const uint8_t* pay;
 
-    // the 16-bit word at payload offset o (even): slot (o / 16) % 8 of the ring
+    // the 16-bit word at payload offset o (even): slot (o / 16) % 4 of the ring
     __device__ __forceinline__ uint32_t word_at(uint32_t o) const {
-        return reinterpret_cast<const uint16_t*>(g_smem)[(roff | (o & 126u)) >> 1];
+        return reinterpret_cast<const uint16_t*>(g_smem)[(roff | (o & (kRingBytesPerLane - 2u))) >> 1];
     }
 
     __device__ __forceinline__ void stage_chunk() {
@@ -173,22 +180,28 @@ struct Lane {
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
         next = word_at(a);
     }
-    // Block boundary (see top_up below): stage at most one chunk for this lane
-    // and report whether the block's reads are not yet known to be complete.
-    // Each block commits one cp.async group per thread, so chunk c < issued
-    // was staged at least issued - 1 - c blocks ago.  A block reads at most 9
-    // words plus, on the escape path, 16 more (chunks up to cpos + 4); when
-    // chunk min(cpos + 4, clast) is at least three blocks old, waiting for
-    // every group but the newest three suffices.
-    __device__ __forceinline__ bool stage_step() {
+    // Top-up point (see top_up below): stage at most two chunks for this lane
+    // and report whether the coming reads are not yet known to be complete.
+    // Top-ups run before every pair of blocks and again after any block that
+    // took the escape path (whose payload words are read from global memory,
+    // so the lane may have moved past chunks never staged).  Each top-up
+    // commits one cp.async group; waiting for every group but the newest then
+    // completes every chunk below `old`, the first chunk staged here.  Two
+    // blocks without escapes read at most 16 words plus the one word read
+    // ahead, payload bytes a .. a + 33, which lie in chunks cpos .. cpos + 2.
+    __device__ __forceinline__ bool stage_pair() {
         const uint32_t cpos = a >> 4;
+        issued = max(issued, cpos);  // chunks an escape payload skipped are never read
+        const uint32_t old = issued;
         const uint32_t target = min(cpos + kRingChunks, clast + 1u);
         if (issued < target) stage_chunk();
-        const uint32_t need = min(cpos + 4u, clast);
-        return a != aend && (int32_t)(issued - 1u - need) < 3;
+        if (issued < target) stage_chunk();
+        const uint32_t need = min(cpos + 2u, clast);
+        return a < aend && need >= old;
     }
     // slow path: stage everything the ring can hold (the caller then waits for all)
     __device__ __forceinline__ void stage_all() {
+        issued = max(issued, a >> 4);
         const uint32_t target = min((a >> 4) + kRingChunks, clast + 1u);
         while (issued < target) stage_chunk();
     }
@@ -209,31 +222,45 @@ struct Lane {
         renorm();
         return e;
     }
-    // one uniform byte (f = 16, cum = 16 * byte)
+    // one uniform byte (f = 16, cum = 16 * byte) of an escape payload; its
+    // renormalisation words come straight from global memory, so the ring
+    // need not hold them.  A lane that runs past its last word (a corrupt
+    // stream) reads zeros and fails the lane end check.
     __device__ __forceinline__ uint32_t byte() {
         const uint32_t slot = x & (kProbScale - 1);
         x = 16u * (x >> kProbBits) + (slot & 15u);
-        renorm();
+        if (x < kRansL) {
+            x = (x << 16) | next;
+            a += 2u;
+            next = a < aend ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(pay + a)) : 0u;
+        }
         return slot >> 4;
     }
 };
 
-// Block-boundary top-up of the NL lanes a thread decodes: one cp.async group
-// per block; if any lane of the warp might read a chunk that is not known to
-// be complete, stage all and wait for everything (rare: bursts of escapes,
-// short lanes), otherwise wait only for groups at least three blocks old.
+// Stage everything the NL lanes' rings can hold and wait for all of it.
+template <int NL>
+__device__ __forceinline__ void stage_all_wait(Lane (&ln)[NL]) {
+#pragma unroll
+    for (int i = 0; i < NL; i++) ln[i].stage_all();
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Top-up of the NL lanes a thread decodes, before every pair of blocks (and
+// after a block with escapes): one cp.async group per top-up; if any lane of
+// the warp might read a chunk that is not known to be complete, stage all and
+// wait for everything (rare: lane starts and ends), otherwise wait for every
+// group but the one just committed.
 template <int NL>
 __device__ __forceinline__ void top_up(Lane (&ln)[NL]) {
     bool urgent = false;
 #pragma unroll
-    for (int i = 0; i < NL; i++) urgent |= ln[i].stage_step();
+    for (int i = 0; i < NL; i++) urgent |= ln[i].stage_pair();
     asm volatile("cp.async.commit_group;" ::: "memory");
     if (__any_sync(0xffffffffu, urgent)) {
-#pragma unroll
-        for (int i = 0; i < NL; i++) ln[i].stage_all();
-        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        stage_all_wait<NL>(ln);
     } else {
-        asm volatile("cp.async.wait_group 3;" ::: "memory");
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
     }
 }
 
@@ -376,10 +403,11 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
     bool esc_bad[NL];
 #pragma unroll
     for (int i = 0; i < NL; i++) {
-        T[i].setup(a, grp0 + i, ln[i], ring_off + 128u * i, status);
+        T[i].setup(a, grp0 + i, ln[i], ring_off + kRingBytesPerLane * i, status);
         esc_bad[i] = false;
     }
 
+    bool slow_prev = false;  // warp-uniform: the previous block took the escape path
     for (int slab = 0; slab < kSlabs; slab++) {
         int64_t eoff[NL];
         bool col_in[NL];  // the slab's block lies inside the true columns
@@ -391,7 +419,7 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
 #pragma unroll 2
         for (int row = 0; row < kTileRows; row++) {
             const int j = slab * kTileRows + row;
-            top_up<NL>(ln);
+            if ((row & 1) == 0 || slow_prev) top_up<NL>(ln);
             if constexpr (is_lossless(KIND)) {
                 uint32_t e[NL][8];
 #pragma unroll
@@ -491,6 +519,10 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
                 any |= esc[i];
             }
             const bool slow = __any_sync(0xffffffffu, any);
+            slow_prev = slow;
+            // no copy may still be in flight into a ring slot that the next
+            // top-up refills after the payload moved the lanes on
+            if (slow) asm volatile("cp.async.wait_group 0;" ::: "memory");
 #pragma unroll
             for (int i = 0; i < NL; i++) {
                 float y[8];
@@ -556,11 +588,9 @@ __device__ __forceinline__ void copy_row_scales(const DecodeArgs& a, int64_t fir
 
 // Shared-memory layout of a decode CTA (g_smem, 128-byte aligned): n_ctx slot
 // tables (16 KB each), the n_ctx x 256 frequency and cumulative-frequency
-// scratch of the table build, then one 128-byte word ring per thread.
-constexpr size_t kRingBytes = (size_t)kThreads * 128;
-
-__host__ __device__ constexpr size_t decode_smem_bytes(int n_ctx) {
-    return (size_t)n_ctx * (kSlots + 512) * 4 + kRingBytes;
+// scratch of the table build, then one 64-byte word ring per lane.
+__host__ __device__ constexpr size_t decode_smem_bytes(int n_ctx, int nl) {
+    return (size_t)n_ctx * (kSlots + 512) * 4 + (size_t)cta_threads(nl) * nl * kRingBytesPerLane;
 }
 
 // byte offset of this thread's first ring in g_smem (a thread running NL
@@ -568,7 +598,7 @@ __host__ __device__ constexpr size_t decode_smem_bytes(int n_ctx) {
 // of n_ctx contexts (18432 bytes each, a multiple of 128)
 template <int NL>
 __device__ __forceinline__ uint32_t lane_ring(int n_ctx) {
-    return (uint32_t)n_ctx * (kSlots + 512) * 4 + 128u * NL * threadIdx.x;
+    return (uint32_t)n_ctx * (kSlots + 512) * 4 + kRingBytesPerLane * NL * threadIdx.x;
 }
 
 // Lanes per thread (NL): two interleaved lanes per thread (512 threads) give
@@ -582,7 +612,7 @@ __device__ __forceinline__ uint32_t lane_ring(int n_ctx) {
 // Tile groups are dealt round-robin over the CTAs first (group g goes to CTA
 // g % gridDim.x), so a small matrix still spreads over every SM.
 template <int KIND, bool DUMP, int NL, bool RAGGED>
-__global__ void __launch_bounds__(kThreads / NL, 1) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(cta_threads(NL), 1) decode_kernel(const DecodeArgs a) {
     uint32_t* const smem = g_smem;
     uint32_t* tab = smem;                    // n_ctx x 4096
     uint32_t* fr = smem + a.n_ctx * kSlots;  // n_ctx x 256
@@ -616,8 +646,8 @@ struct BatchCounters {
 constexpr uint32_t kWaitSpins = 1u << 23;  // x ~256 ns sleep: about 2 s before giving up
 
 constexpr int kBatchNL = 2;                              // lanes per thread in the batched kernel
-constexpr int kBatchThreads = kThreads / kBatchNL;      // 512
-constexpr int kGroupsPerUnit = kThreads / 32;           // 32 groups: one per warp and lane slot
+constexpr int kBatchThreads = cta_threads(kBatchNL);    // 640: 20 warps
+constexpr int kGroupsPerUnit = kBatchThreads / 32 * kBatchNL;  // 40 groups: one per warp and lane slot
 
 template <int KIND, bool RAGGED>
 __global__ void __launch_bounds__(kBatchThreads, 1)
@@ -679,7 +709,8 @@ __global__ void __launch_bounds__(kBatchThreads, 1)
 }
 
 // ------------------------------------------------------------ launching
-constexpr size_t kMaxSmem = decode_smem_bytes(kLossyContexts);
+constexpr size_t kBatchSmem = decode_smem_bytes(kLossyContexts, kBatchNL);
+constexpr size_t kMaxSmem = decode_smem_bytes(kLossyContexts, 1) > kBatchSmem ? decode_smem_bytes(kLossyContexts, 1) : kBatchSmem;
 
 struct DeviceInfo {
     int sms = 0;
@@ -696,36 +727,45 @@ DeviceInfo device_info() {
     return cache[dev];
 }
 
+// cudaFuncSetAttribute applies to the calling thread's current device only:
+// raise a kernel's dynamic shared-memory limit once per device (bit d of
+// *done records device d; setting it twice is harmless).
+ep_status raise_smem_limit(const void* kernel, std::atomic<uint64_t>* done) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return EP_ERR_CUDA;
+    const uint64_t bit = 1ull << dev;
+    if (done->load(std::memory_order_acquire) & bit) return EP_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem) != cudaSuccess)
+        return EP_ERR_CUDA;
+    done->fetch_or(bit, std::memory_order_release);
+    return EP_OK;
+}
+
 template <int KIND, bool DUMP, int NL, bool RAGGED>
-ep_status launch_nl(const DecodeArgs& a, size_t smem, cudaStream_t stream) {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(decode_kernel<KIND, DUMP, NL, RAGGED>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
-    });
-    if (attr_err != cudaSuccess) return EP_ERR_CUDA;
+ep_status launch_nl(const DecodeArgs& a, cudaStream_t stream) {
+    static std::atomic<uint64_t> done{0};
+    if (raise_smem_limit(reinterpret_cast<const void*>(decode_kernel<KIND, DUMP, NL, RAGGED>), &done) != EP_OK)
+        return EP_ERR_CUDA;
     const int64_t jobs = ((a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp + NL - 1) / NL;
     const int64_t cap = device_info().sms;
     const int grid = (int)(jobs < cap ? jobs : cap);
-    decode_kernel<KIND, DUMP, NL, RAGGED><<<grid, kThreads / NL, smem, stream>>>(a);
+    decode_kernel<KIND, DUMP, NL, RAGGED><<<grid, cta_threads(NL), decode_smem_bytes(a.n_ctx, NL), stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 
 bool is_ragged(int64_t rows, int64_t cols) { return (rows % kTileRows) != 0 || (cols % kTileCols) != 0; }
 
 template <int KIND, bool DUMP, bool RAGGED>
-ep_status launch_r(const DecodeArgs& a, size_t smem, cudaStream_t stream) {
+ep_status launch_r(const DecodeArgs& a, cudaStream_t stream) {
     const int64_t groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
     if (DUMP || groups <= (int64_t)device_info().sms * (kThreads / 32))
-        return launch_nl<KIND, DUMP, 1, RAGGED>(a, smem, stream);
-    return launch_nl<KIND, DUMP, 2, RAGGED>(a, smem, stream);
+        return launch_nl<KIND, DUMP, 1, RAGGED>(a, stream);
+    return launch_nl<KIND, DUMP, 2, RAGGED>(a, stream);
 }
 
 template <int KIND, bool DUMP>
-ep_status launch(const DecodeArgs& a, size_t smem, cudaStream_t stream) {
-    return is_ragged(a.rows, a.cols) ? launch_r<KIND, DUMP, true>(a, smem, stream)
-                                     : launch_r<KIND, DUMP, false>(a, smem, stream);
+ep_status launch(const DecodeArgs& a, cudaStream_t stream) {
+    return is_ragged(a.rows, a.cols) ? launch_r<KIND, DUMP, true>(a, stream) : launch_r<KIND, DUMP, false>(a, stream);
 }
 
 constexpr size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -787,19 +827,14 @@ int kind_of(const Layout& L) {
 
 template <int KIND, bool RAGGED>
 ep_status launch_batch_r(const ep_batch_plan* p, uint32_t* d_status, cudaStream_t stream) {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(batch_kernel<KIND, RAGGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kMaxSmem);
-    });
-    if (attr_err != cudaSuccess) return EP_ERR_CUDA;
+    static std::atomic<uint64_t> done{0};
+    if (raise_smem_limit(reinterpret_cast<const void*>(batch_kernel<KIND, RAGGED>), &done) != EP_OK)
+        return EP_ERR_CUDA;
     uint8_t* ws = static_cast<uint8_t*>(p->d_workspace);
-    const size_t smem = decode_smem_bytes(kLossyContexts);
     const int64_t cap = device_info().sms;
     const int grid = (int)(p->total_units < cap ? p->total_units : cap);
     if (grid <= 0) return EP_OK;
-    batch_kernel<KIND, RAGGED><<<grid, kBatchThreads, smem, stream>>>(
+    batch_kernel<KIND, RAGGED><<<grid, kBatchThreads, kBatchSmem, stream>>>(
         reinterpret_cast<const DecodeArgs*>(ws + p->items_off), reinterpret_cast<const int64_t*>(ws + p->units_off),
         p->n_items, p->ring, reinterpret_cast<BatchCounters*>(ws + p->counters_off), d_status);
     return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
@@ -813,17 +848,15 @@ ep_status launch_batch(const ep_batch_plan* p, uint32_t* d_status, cudaStream_t 
 
 ep_status launch_parsed(const Layout& L, const DecodeArgs& a, bool dump, uint32_t* d_status, cudaStream_t stream) {
     if (cudaMemsetAsync(d_status, 0, sizeof(uint32_t), stream) != cudaSuccess) return EP_ERR_CUDA;
-    const size_t smem = decode_smem_bytes(L.n_ctx);
     switch (kind_of(L)) {
-        case K_BF16: return dump ? launch<K_BF16, true>(a, smem, stream) : launch<K_BF16, false>(a, smem, stream);
-        case K_FP16: return dump ? launch<K_FP16, true>(a, smem, stream) : launch<K_FP16, false>(a, smem, stream);
-        case K_FP8: return dump ? launch<K_FP8, true>(a, smem, stream) : launch<K_FP8, false>(a, smem, stream);
-        case K_INT8: return dump ? launch<K_INT8, true>(a, smem, stream) : launch<K_INT8, false>(a, smem, stream);
-        case K_LOSSLESS8:
-            return dump ? launch<K_LOSSLESS8, true>(a, smem, stream) : launch<K_LOSSLESS8, false>(a, smem, stream);
+        case K_BF16: return dump ? launch<K_BF16, true>(a, stream) : launch<K_BF16, false>(a, stream);
+        case K_FP16: return dump ? launch<K_FP16, true>(a, stream) : launch<K_FP16, false>(a, stream);
+        case K_FP8: return dump ? launch<K_FP8, true>(a, stream) : launch<K_FP8, false>(a, stream);
+        case K_INT8: return dump ? launch<K_INT8, true>(a, stream) : launch<K_INT8, false>(a, stream);
+        case K_LOSSLESS8: return dump ? launch<K_LOSSLESS8, true>(a, stream) : launch<K_LOSSLESS8, false>(a, stream);
         case K_LOSSLESS32:
-            return dump ? launch<K_LOSSLESS32, true>(a, smem, stream) : launch<K_LOSSLESS32, false>(a, smem, stream);
-        default: return dump ? launch<K_LOSSLESS, true>(a, smem, stream) : launch<K_LOSSLESS, false>(a, smem, stream);
+            return dump ? launch<K_LOSSLESS32, true>(a, stream) : launch<K_LOSSLESS32, false>(a, stream);
+        default: return dump ? launch<K_LOSSLESS, true>(a, stream) : launch<K_LOSSLESS, false>(a, stream);
     }
 }
 
