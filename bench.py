@@ -567,6 +567,19 @@ def bench_allocation(ep, synth, torch, np, device, stream, avg_bpp: float = 4.0)
     return res
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (from /proc/cpuinfo), or the platform's processor string."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
 def cpu_baseline(blobs, shapes, n_layers):
     import oracle
     sample = blobs[:n_layers]
@@ -576,7 +589,8 @@ def cpu_baseline(blobs, shapes, n_layers):
     for b in sample:
         oracle.decode_threaded(b, threads)
     dt = time.perf_counter() - t
-    return {"value": params / dt / 1e9, "unit": "G params/s", "cores": threads, "kind": "oracle",
+    return {"value": params / dt / 1e9, "unit": "G params/s", "cores": threads, "cpu_model": cpu_model(),
+            "kind": "oracle",
             "sample": f"first {n_layers} layers ({params / 1e6:.0f} M params) of the same model, decoded to BF16 by "
                       f"the plain C oracle on {threads} host threads (contiguous tile ranges)",
             "seconds": dt}
@@ -609,8 +623,8 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "u32 rANS + fp64/fp32 reconstruction -> bf16",
             "data": "synthetic (seeded Student-t nu=5, std 0.02)",
             "config": {"workload": f"whole-model decode sample on the CPU oracle: {sample}"},
-            "cpu_baseline": {"value": value, "unit": "G params/s", "cores": threads, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "G params/s", "cores": threads, "cpu_model": cpu_model(),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "G params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

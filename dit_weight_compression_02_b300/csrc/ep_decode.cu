@@ -1,8 +1,8 @@
 // GPU decode of EntroPack streams on B300 (sm_103a): fused rANS symbol
 // decoding, E8 reconstruction, row rescaling and container conversion
 // ("EntroPack: Fast and Accurate Entropy-Coded Weight Compression at Arbitrary
-// Bitrates", Abstract: "fast, fused symbol decoding and numerical weight
-// reconstruction on the GPU"; containers BF16, FP16, FP8, INT8).
+// Bitrates", Abstract: the symbols are decoded and the weight values rebuilt
+// in one pass on the GPU; containers BF16, FP16, FP8, INT8).
 //
 // Work decomposition.  A tile (32 x 128 weights) carries 4 independent rANS
 // lanes; thread (tig, l) of a warp runs lane l of tile tig, so one warp
@@ -1037,6 +1037,12 @@ extern "C" ep_status ep_batch_decode_static(const ep_batch_item* items, int64_t 
     ep_status st = static_scratch_address(&ws);
     if (st != EP_OK) return st;
     const size_t units_off = batch_units_off(n_items), ctr_off = batch_ctr_off(n_items);
+    // Host threads calling at the same time would interleave their copies
+    // into the one array: hold the array from the first copy to the launch.
+    // Each call's copies and kernel then follow one another on its stream;
+    // calls on different streams can still overlap on the GPU (see the header).
+    static std::mutex array_mu;
+    std::lock_guard<std::mutex> hold(array_mu);
 
     // Validate every stream and stage the descriptors in fixed-size host
     // chunks on this thread's stack; each chunk goes to the device array with

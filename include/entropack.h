@@ -5,12 +5,12 @@
  * encoder that produces the stream.
  *
  * Method: "EntroPack: Fast and Accurate Entropy-Coded Weight Compression at
- * Arbitrary Bitrates", Abstract -- row-normalised E8 lattice quantisation, a
- * conditional probability model of lattice coordinates, sampled storage
- * estimates to select the quantisation resolution, entropy coding in
- * independently decodable tiles, fused symbol decoding and weight
- * reconstruction on the GPU, containers BF16/FP16/FP8/INT8 with the storage
- * bitrate independent of the container.
+ * Arbitrary Bitrates", Abstract -- E8 lattice quantisation of rows scaled to
+ * unit size, a probability model of each lattice coordinate given the coset,
+ * a resolution picked from rate estimates on sampled rows, entropy coding in
+ * tiles that decode independently, one GPU pass that decodes the symbols and
+ * rebuilds the weights, and BF16/FP16/FP8/INT8 containers whose precision is
+ * chosen apart from the storage rate.
  * API surface: "EntroPack PyTorch Guide: Lossless Weights, Bitrates and Memory
  * Checks", sections "Choose a compression contract" (lossy target bitrate vs
  * lossless tiled ANS; compress / decompress), "Start with a tensor round trip"
@@ -126,8 +126,8 @@ ep_status ep_encode_at(const void *w, int64_t rows, int64_t cols, const ep_param
                        size_t *blob_bytes);
 
 /*
- * The sampled storage estimate ("Sampled storage estimates select the
- * quantization resolution without repeated full-stream encoding", Abstract)
+ * The sampled storage estimate (Abstract: the resolution is chosen from rate
+ * estimates on a sample, not by encoding the whole stream again and again)
  * of a BF16 matrix (host) at index j: coded bits per parameter on the strided
  * row sample (sample_frac <= 0 selects 0.05), the figure the rate search
  * steers.  *j_min (may be NULL) receives the smallest admissible index.
@@ -164,12 +164,18 @@ ep_status ep_allocate_bits(const ep_layer_ref *layers, int64_t n_layers, float a
 
 /* 8 * bytes / (rows * cols) after validating the stream ("actual_bpp", metadata included). */
 ep_status ep_actual_bpp(const uint8_t *blob, size_t bytes, double *bpp);
-/* Parse and fully validate a host copy of a stream. */
+/* Parse and fully validate a host copy of a stream and report its metadata
+ * (shape, mode, container, resolution, sizes).  Serves the guide's advice,
+ * when a restore fails, to compare the configuration and metadata on both
+ * sides of the round trip and to check that the stored object carries all
+ * that the decoder needs ("EntroPack PyTorch Guide", "Diagnose compression
+ * failures in the correct order").  Errors: EP_ERR_INVALID_ARG (NULL),
+ * EP_ERR_CORRUPT (any inconsistent header field, table, offset or size). */
 ep_status ep_query(const uint8_t *blob, size_t bytes, ep_info *out);
 
 /*
- * Decode a stream on the GPU ("fused symbol decoding and numerical weight
- * reconstruction on the GPU", Abstract).
+ * Decode a stream on the GPU (Abstract: symbol decoding and the rebuilding of
+ * the weight values run fused, on the GPU).
  *   d_out            rows x cols container elements, row-major, 16-byte aligned
  *   d_row_scale_out  FP8/INT8 lossy streams: rows floats t_r such that
  *                    weight[r, k] ~= t_r * d_out[r, k]; NULL allowed (and
@@ -215,8 +221,8 @@ ep_status ep_decode_h(const ep_stream_handle *h, const void *d_blob, void *d_out
 /*
  * Batched decode: many streams (e.g. every linear layer of a model) in one
  * persistent launch.  All items must share mode and container.  Work is cut
- * into units of 32 groups of 8 tiles (256 tiles) of one item; CTAs (one per
- * SM) claim units in item order, one warp per group.
+ * into units of 40 groups of 8 tiles (320 tiles) of one item; CTAs (one per
+ * SM, 20 warps) claim units in item order, two groups per warp.
  *
  *   ring == 0  every item writes its own d_out (outputs must not overlap);
  *   ring == R  item i may reuse the output buffer of item i - R ("decode back
@@ -277,7 +283,13 @@ typedef enum {
                                        L2-resident workspace is faster */
 } ep_linear_mode;
 
-/* Dense BF16 GEMM (uncompressed W): the tensor-core kernel used by ep_compressed_linear. */
+/* Dense BF16 GEMM (uncompressed W): the tensor-core kernel used by
+ * ep_compressed_linear, exported so that a compressed layer can be compared
+ * with its uncompressed original on the same inputs and the same kernel (the
+ * guide keeps an uncompressed baseline beside every compressed result:
+ * "EntroPack PyTorch Guide", "Measure memory with clear boundaries" and
+ * "Test saved artifacts and reloads before deployment").  Arguments, layout
+ * and errors as ep_compressed_linear, with W given as rows x cols BF16. */
 ep_status ep_linear_bf16(const uint16_t *d_x, const uint16_t *d_w, uint16_t *d_y, const uint16_t *d_bias,
                          int64_t tokens, int64_t rows, int64_t cols, uint32_t *d_status, ep_stream_t stream);
 
@@ -318,8 +330,11 @@ ep_status ep_compressed_linear_h(const ep_stream_handle *h, const void *d_blob, 
  *  - The first call on a device looks up the array's device address with
  *    cudaGetSymbolAddress (with that device current) and caches it; make that
  *    first call before any stream capture.
- *  - Every call shares the one array: calls whose work overlaps on the GPU
- *    (for example on two streams) race and must be serialised by the caller.
+ *  - Every call shares the one array.  Host threads that call at the same
+ *    time are serialised inside the library from the first copy to the
+ *    launch, so calls on one stream run one after another.  Calls whose work
+ *    overlaps on the GPU (for example on two streams) race on the array and
+ *    must be serialised by the caller.
  */
 #define EP_BATCH_STATIC_MAX_ITEMS 1024
 ep_status ep_batch_decode_static(const ep_batch_item *items, int64_t n_items, int32_t ring, uint32_t *d_status,
@@ -383,7 +398,12 @@ ep_status ep_fp8_row_encode(const uint16_t *w, int64_t rows, int64_t cols, uint8
 ep_status ep_fp8_row_decode(const uint8_t *d_codes, const float *d_scales, int64_t rows, int64_t cols,
                             uint16_t *d_out, ep_stream_t stream);
 
-/* Synchronise `stream` and map the status word: 0 -> EP_OK, any bit -> EP_ERR_CORRUPT. */
+/* Synchronise `stream` and map the status word: 0 -> EP_OK, any bit ->
+ * EP_ERR_CORRUPT.  A decode that the device found corrupt must stop with a
+ * clear error rather than hand back a partly converted tensor ("EntroPack
+ * PyTorch Guide", "Test saved artifacts and reloads before deployment":
+ * partial failures end in a clear error).  EP_ERR_INVALID_ARG for a NULL
+ * status word, EP_ERR_CUDA if the copy or the synchronisation fails. */
 ep_status ep_sync_status(const uint32_t *d_status, ep_stream_t stream);
 
 #ifdef __cplusplus

@@ -1079,7 +1079,7 @@ void oracle_gemm_f64(const double *x, const double *w, double *y, int64_t T, int
    The comparators of the evaluation ("EntroPack: Fast and Accurate
    Entropy-Coded Weight Compression at Arbitrary Bitrates", Abstract: lower
    relative L2 weight error than NF4 at a 4-bit target, with less storage;
-   lower errors than fixed-width formats at comparable storage).
+   lower errors than fixed-width codes of about the same size).
 
    Both are block-absmax 4-bit codebook quantisers: a block of `block`
    consecutive weights stores its absolute maximum s as FP32 and one 4-bit

@@ -6,15 +6,15 @@
  * Method passages followed ("EntroPack: Fast and Accurate Entropy-Coded
  * Weight Compression at Arbitrary Bitrates", Abstract):
  *   row-normalised E8 lattice quantisation        -> oracle_row_rms, oracle_e8_nearest
- *   conditional probability model of coordinates  -> oracle_block_symbols
- *   sampled storage estimates select resolution   -> oracle_estimate_bpp, oracle_select_j
+ *   coordinate probability model given the coset  -> oracle_block_symbols
+ *   resolution picked from sampled rate estimates -> oracle_estimate_bpp, oracle_select_j
  *   entropy coding in independently decodable tiles -> oracle_rans_*, oracle_encode
  *   fused decode + reconstruction into BF16/FP16/FP8/INT8 -> oracle_decode
  * Lossless tiled ANS ("EntroPack PyTorch Guide", section "Choose a
  * compression contract", TileANSConfig) -> oracle_encode_lossless.
  * Comparators of the evaluation (Abstract: lower relative L2 weight error
- * than NF4 at a 4-bit target, with less storage, and than fixed-width formats
- * at comparable storage) -> oracle_q4_roundtrip with oracle_nf4_levels /
+ * than NF4 at a 4-bit target, with less storage, and than fixed-width codes
+ * of about the same size) -> oracle_q4_roundtrip with oracle_nf4_levels /
  * oracle_int4_levels, oracle_fp8_row_roundtrip.
  * The stream layout and every constant are this repository's readings of
  * those passages (stream format version 1).

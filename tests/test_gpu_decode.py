@@ -308,7 +308,9 @@ def test_c3_whole_model_in_bench_configuration(ep):
     all 1,296,000 tiles ended at x = L having consumed exactly its words, and
     no tile or escape check fired.  The ring's final contents (the last 16
     layers) are compared bit for bit with the oracle on sampled tile rows: the
-    first, a middle and the last of each layer.
+    first, a middle and the last of each layer.  Then all 210 layers are
+    decoded again by one batched launch into distinct buffers and every value
+    of every layer is compared with the oracle.
     """
     shapes = []
     for _ in range(30):
@@ -329,6 +331,15 @@ def test_c3_whole_model_in_bench_configuration(ep):
             y_o, _ = oracle.decode(blobs[i], tr * tpr, (tr + 1) * tpr)
             rows = slice(tr * 32, tr * 32 + 32)
             assert (g[rows] == y_o[rows]).all(), (i, tr)
+    del bufs, outs, bd
+    # every layer, every value: the same batched launch with a distinct output
+    # per layer (10.6 GB of BF16 in HBM), each layer compared with the
+    # oracle's decode of it, one layer at a time to bound host memory
+    outs = [torch.empty((r, c), dtype=torch.bfloat16, device="cuda") for r, c in shapes]
+    ep.BatchDecoder(dbs, outs, ring=0)()
+    for i, b in enumerate(blobs):
+        assert (_np(outs[i]) == oracle.decode_threaded(b)[0]).all(), i
+        outs[i] = None
 
 
 def test_streaming_decoder_uploads_and_decodes(ep):

@@ -3,7 +3,7 @@
 The comparators are the formats EntroPack is measured against ("EntroPack:
 Fast and Accurate Entropy-Coded Weight Compression at Arbitrary Bitrates",
 Abstract: lower relative L2 weight error than NF4 at a 4-bit target, with less
-storage; lower error than fixed-width formats at comparable storage).  Pins:
+storage; lower error than fixed-width codes of about the same size).  Pins:
 * the NF4 levels through the normal CDF (scipy, not the oracle's bisection):
   equal probability steps, 7 negative and 8 positive levels, the offset d;
 * the 4-bit quantiser against a brute-force numpy restatement on small

@@ -6,8 +6,10 @@ owns every allocation, latency-critical paths where cudaMalloc would stall)
 use this entry point; its scratch lives in a device array inside the
 library.  The test calls it through the C ABI twice in a row, with two
 different sets of streams, and compares each result bit for bit with the
-workspace-based entry point (ep_batch_prepare + ep_batch_decode), which the
-other GPU tests check against the CPU oracle.  It also checks that an
+workspace-based entry point (ep_batch_prepare + ep_batch_decode) and with the
+CPU oracle's decode of the same streams.  A third call passes more streams
+than the entry point stages per host chunk, so the descriptor and unit-table
+copies at nonzero offsets are exercised too.  It also checks that an
 oversized batch is refused before any work is enqueued.
 
 The file name sorts last so that a run which stops at the first failure has
@@ -19,6 +21,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -61,12 +64,14 @@ def _bits(t):
 def test_static_batch_matches_workspace_entry_twice(ep):
     # call 1: seven layers of one transformer block with distinct outputs
     shapes1 = [(512, 3840)] * 4 + [(1024, 3840)] * 2 + [(512, 1024)]
-    blobs1 = [ep.DeviceBlob(ep.encode(synth.student_t5_bf16(300 + i, r, c), 4.0)) for i, (r, c) in enumerate(shapes1)]
+    host1 = [oracle.encode(synth.student_t5_bf16(300 + i, r, c), 4.0) for i, (r, c) in enumerate(shapes1)]
+    blobs1 = [ep.DeviceBlob(b) for b in host1]
     ref1 = _workspace_call(ep, blobs1, 0, shapes1)
     outs1 = [torch.full(s, 7.0, dtype=torch.bfloat16, device="cuda") for s in shapes1]
     _static_call(ep, blobs1, outs1, ring=0)
-    for a, b in zip(outs1, ref1):
+    for a, b, h in zip(outs1, ref1, host1):
         assert (_bits(a) == _bits(b)).all()
+        assert (_bits(a).view(np.uint16) == oracle.decode(h)[0]).all()
 
     # call 2: a different batch (ragged tile groups, a ring of two reused
     # buffers), so the array's leftover descriptors and counters from call 1
@@ -79,6 +84,22 @@ def test_static_batch_matches_workspace_entry_twice(ep):
     for k in range(2):
         last = max(i for i in range(len(blobs2)) if i % 2 == k)
         assert (_bits(ring_bufs[k]) == _bits(ref2[last])).all()
+        assert (_bits(ring_bufs[k]).view(np.uint16) == oracle.decode(blobs2[last].host.numpy().tobytes())[0]).all()
+
+
+def test_static_batch_more_items_than_one_host_chunk(ep):
+    # 57 small streams: the entry point stages descriptors 32 at a time, so the
+    # second chunk's copies land at a nonzero offset of the array, and the
+    # unit table's final entry is written after both chunks
+    shapes = [(32 * (1 + i % 3), 128 * (1 + i % 4)) for i in range(57)]
+    host = [oracle.encode(synth.normal_bf16(700 + i, r, c), 3.0 + 0.5 * (i % 3)) for i, (r, c) in enumerate(shapes)]
+    blobs = [ep.DeviceBlob(b) for b in host]
+    ref = _workspace_call(ep, blobs, 0, shapes)
+    outs = [torch.full(s, -1.0, dtype=torch.bfloat16, device="cuda") for s in shapes]
+    _static_call(ep, blobs, outs, ring=0)
+    for a, b, h in zip(outs, ref, host):
+        assert (_bits(a) == _bits(b)).all()
+        assert (_bits(a).view(np.uint16) == oracle.decode(h)[0]).all()
 
 
 def test_static_batch_rejects_oversized_batch(ep):
