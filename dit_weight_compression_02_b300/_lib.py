@@ -71,6 +71,7 @@ SIGNATURES = {
     "ep_stream_close": (None, [P]),
     "ep_decode_h": (i32, [P, P, P, P, P, P]),
     "ep_compressed_linear_h": (i32, [P, P, P, i64, P, P, i32, P, sz, P, P]),
+    "ep_fused_tokens_per_pass": (i64, [i64]),
     "ep_q4_levels": (i32, [i32, P]),
     "ep_q4_encode": (i32, [P, i64, i64, P, P, P, i32]),
     "ep_q4_decode": (i32, [P, P, i64, i64, P, P, P]),

@@ -354,7 +354,13 @@ def linear_bf16(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = Non
 def compressed_linear(db: DeviceBlob, x: torch.Tensor, mode: int = LINEAR_DECODE_THEN_GEMM,
                       out: torch.Tensor | None = None, workspace: torch.Tensor | None = None, status=None,
                       stream=None, bias: torch.Tensor | None = None):
-    """ep_compressed_linear: Y = X W^T (+ bias) with W decoded from `db` by the library's kernels."""
+    """ep_compressed_linear: Y = X W^T (+ bias) with W decoded from `db` by the library's kernels.
+
+    mode LINEAR_DECODE_THEN_GEMM decodes W into a BF16 workspace and runs the
+    tensor-core GEMM on it; LINEAR_FUSED decodes W straight into shared memory
+    as the tensor-core operand (no workspace; in_features % 128 == 0; tokens in
+    passes of fused_tokens_per_pass(in_features), each decoding W again).
+    """
     _check_bf16_2d(x, "x")
     rows, cols = db.shape
     if x.shape[1] != cols:
@@ -372,6 +378,11 @@ def compressed_linear(db: DeviceBlob, x: torch.Tensor, mode: int = LINEAR_DECODE
     if status is None:
         sync_status(st, stream)
     return y
+
+
+def fused_tokens_per_pass(in_features: int) -> int:
+    """ep_fused_tokens_per_pass: tokens one fused pass covers (0: the shape is not served)."""
+    return int(lib.ep_fused_tokens_per_pass(int(in_features)))
 
 
 # ------------------------------------------------- fixed-width comparators
@@ -573,7 +584,7 @@ def compress_linears(linears: dict, avg_bpp: float, sensitivities: dict | None =
 
 __all__ = ["encode", "query", "actual_bpp", "DeviceBlob", "decode", "decode_into", "sync_status", "BatchDecoder",
            "StreamingDecoder",
-           "linear_bf16", "compressed_linear", "LINEAR_DECODE_THEN_GEMM", "LINEAR_FUSED",
+           "linear_bf16", "compressed_linear", "fused_tokens_per_pass", "LINEAR_DECODE_THEN_GEMM", "LINEAR_FUSED",
            "EntroPackLossyConfig", "TileANSConfig", "CompressedTensor", "compress", "decompress",
            "CompressedLinear", "EntroPackError", "CONTAINERS", "CONTAINER_DTYPES",
            "q4_levels", "q4_encode", "q4_decode", "Q4Tensor", "Q4_KINDS", "fp8_row_encode", "fp8_row_decode",

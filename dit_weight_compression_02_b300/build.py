@@ -23,7 +23,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "libentropack.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
-CU_SOURCES = ["ep_decode.cu", "ep_linear.cu", "ep_q4.cu"]
+CU_SOURCES = ["ep_decode.cu", "ep_linear.cu", "ep_fused.cu", "ep_q4.cu"]
 CXX_SOURCES = ["ep_host.cpp", "ep_encode.cpp", "ep_q4.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

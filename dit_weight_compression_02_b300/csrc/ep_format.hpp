@@ -62,6 +62,14 @@ ep_status parse_and_validate(const uint8_t* blob, size_t bytes, Layout* out);
 ep_status decode_parsed(const Layout& L, const void* d_blob, void* d_out, float* d_row_scale, uint32_t* d_status,
                         ep_stream_t stream);
 
+// Fused CompressedLinear (ep_fused.cu): Y = X W^T (+ b) with W decoded
+// straight into shared memory, in passes of fused_tokens_per_pass(cols)
+// tokens (0: the shape is not served).  L is a validated lossy BF16 stream;
+// the caller has checked pointers and shapes.  d_status is zeroed first.
+int64_t fused_tokens_per_pass(int64_t cols);
+ep_status fused_linear_parsed(const Layout& L, const void* d_blob, const uint16_t* d_x, int64_t tokens,
+                              uint16_t* d_y, const uint16_t* d_bias, uint32_t* d_status, ep_stream_t stream);
+
 inline size_t container_bytes(int container) {
     return container == EP_C_FP32 ? 4 : (container >= EP_C_FP8_E4M3 ? 1 : 2);
 }

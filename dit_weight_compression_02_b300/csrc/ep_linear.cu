@@ -312,6 +312,13 @@ ep_status compressed_linear_parsed(const Layout& L, const void* d_blob, const ui
                                    uint32_t* d_status, ep_stream_t stream) {
     ep_status st;
     if (L.mode != EP_MODE_LOSSY_E8 || L.container != EP_C_BF16) return EP_ERR_UNSUPPORTED;
+    if (mode == EP_LINEAR_FUSED) {
+        // W never leaves the chip: no workspace
+        if (fused_tokens_per_pass(L.cols) <= 0) return EP_ERR_UNSUPPORTED;
+        st = check_gemm_args(d_x, d_blob, d_y, d_bias, tokens, L.rows, L.cols, d_status);
+        if (st != EP_OK) return st;
+        return fused_linear_parsed(L, d_blob, d_x, tokens, d_y, d_bias, d_status, stream);
+    }
     if (mode != EP_LINEAR_DECODE_THEN_GEMM) return EP_ERR_UNSUPPORTED;
     const size_t need = (size_t)L.rows * (size_t)L.cols * 2u;
     if (!d_ws || ws_bytes < need) return EP_ERR_INVALID_ARG;

@@ -276,11 +276,11 @@ ep_status ep_batch_decode(const ep_batch_plan *plan, uint32_t *d_status, ep_stre
  */
 typedef enum {
     EP_LINEAR_DECODE_THEN_GEMM = 0, /* decode W into d_ws (rows x cols BF16), then the GEMM */
-    EP_LINEAR_FUSED = 1             /* reserved: W tiles decoded straight into shared memory.  Returns
-                                       EP_ERR_UNSUPPORTED: the accumulator holds at most 512 tokens per
-                                       decoded weight, so W would be decoded tokens / 512 times, and the
-                                       decoded tiles in flight exceed shared memory; decoding once into an
-                                       L2-resident workspace is faster */
+    EP_LINEAR_FUSED = 1             /* W decoded straight into shared memory as the tensor-core operand and
+                                       multiplied there: no workspace (d_ws may be NULL), W never written to
+                                       global memory.  Needs cols % 128 == 0; tokens run in passes of
+                                       ep_fused_tokens_per_pass(cols) (640 for cols = 3840), each decoding W
+                                       again, so it serves few tokens.  EP_ERR_UNSUPPORTED for other shapes */
 } ep_linear_mode;
 
 /* Dense BF16 GEMM (uncompressed W): the tensor-core kernel used by
@@ -308,6 +308,14 @@ ep_status ep_compressed_linear(const uint8_t *h_blob, const void *d_blob, size_t
 ep_status ep_compressed_linear_h(const ep_stream_handle *h, const void *d_blob, const uint16_t *d_x, int64_t tokens,
                                  uint16_t *d_y, const uint16_t *d_bias, int32_t mode, void *d_ws, size_t ws_bytes,
                                  uint32_t *d_status, ep_stream_t stream);
+
+/* Tokens that one pass of EP_LINEAR_FUSED covers for a layer with cols
+ * in_features on the current device (every pass decodes W once); 0 when the
+ * fused mode does not serve the shape.  The decoder's unit is whole tile rows
+ * of W, as many (up to 3) as shared memory holds next to the slot tables; the
+ * tensor-memory accumulators (512 columns, 32 per tile row and 128 tokens)
+ * bound the tokens of a pass. */
+int64_t ep_fused_tokens_per_pass(int64_t cols);
 
 /*
  * Allocation-free variant of ep_batch_prepare + ep_batch_decode.  The pages

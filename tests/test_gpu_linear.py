@@ -124,6 +124,36 @@ def test_compressed_linear_full_size_sampled(ep):
     _check(y, x, w_hat, rows=rows)
 
 
+@pytest.mark.parametrize("T,N,K,with_bias", [(128, 10240, 3840, False), (77, 1000, 1024, True),
+                                              (300, 544, 384, False), (5, 48, 256, True), (700, 256, 1024, False)])
+def test_fused_linear_matches_fp64(ep, T, N, K, with_bias):
+    # W decoded straight into shared memory as the tensor-core operand.  The
+    # shapes cover the CompressedLinear layer at 128 tokens (three tile rows
+    # per CTA, one wave), ragged tile rows (N % 32 != 0), an odd number of
+    # tiles per row (K = 384), several token tiles per pass (T = 300) and two
+    # passes (T = 700 > 640 tokens per pass for K = 1024); the outlier rows
+    # put escapes into every layer
+    w = synth.rows_outliers_bf16(N + K, N, K, frac=0.002, k_sigma=40.0)
+    x = synth.normal_bf16(T + 3 * K, T, K, std=1.0)
+    blob = oracle.encode(w, 4.0)
+    sym = oracle.decode_symbols(blob)
+    assert (sym.reshape(N, -1, 8)[:, :, 1:] == 0).any()  # escaped coordinates exist
+    b = synth.normal_bf16(N, 1, N, std=0.5)[0] if with_bias else None
+    bd = None if b is None else torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    y = ep.compressed_linear(ep.DeviceBlob(blob), _bf16_dev(x), mode=ep.LINEAR_FUSED, bias=bd)
+    assert y.shape == (T, N)
+    _check(y, x, oracle.container_to_f64(oracle.decode(blob)[0], "bf16"), bias_bits=b)
+
+
+def test_fused_linear_unsupported_shapes(ep):
+    assert ep.fused_tokens_per_pass(3840) == 640 and ep.fused_tokens_per_pass(200) == 0
+    w = synth.normal_bf16(66, 64, 200)  # in_features not a multiple of 128
+    db = ep.DeviceBlob(oracle.encode(w, 4.0))
+    with pytest.raises(ep.EntroPackError) as e:
+        ep.compressed_linear(db, _bf16_dev(synth.normal_bf16(67, 8, 200)), mode=ep.LINEAR_FUSED)
+    assert e.value.status == "EP_ERR_UNSUPPORTED"
+
+
 def test_compressed_linear_rejects_bad_args(ep):
     w = synth.normal_bf16(63, 64, 256)
     db = ep.DeviceBlob(oracle.encode(w, 4.0))
