@@ -150,9 +150,11 @@ def job_throughput(units_per_rank: float, steps: int, world: int, elapsed_s: flo
 
 
 def source_sha() -> str:
+    """Hash of the batched decode kernel's sources (the kernel file and its shared device header)."""
     h = hashlib.sha256()
-    with open(os.path.join(ROOT, "dit_weight_compression_02_b300", "csrc", "ep_decode.cu"), "rb") as f:
-        h.update(f.read())
+    for name in ("ep_decode.cu", "ep_decode_dev.cuh"):
+        with open(os.path.join(ROOT, "dit_weight_compression_02_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -362,13 +364,57 @@ def bench_linear(ep, synth, torch, np, device, stream, peaks):
     y_ref = (torch.from_numpy(synth.bf16_to_f32(x_bits[rows])).double() @ w_hat.t()).numpy()
     err = float(np.abs(y_cl[rows] - y_ref).max() / np.abs(y_ref).max())
     peak = peaks.get("bf16_tflops")
+
+    # token sweep: the fused kernel (W decoded straight into shared memory, no
+    # workspace; passes of fused_tokens_per_pass(K) tokens, each decoding W)
+    # against decode-then-GEMM, the same GEMM on dense W and cuBLAS, each on
+    # the first T rows of X; L2 evicted before every timed call
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def timed(fn, reps=7):
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                fn()
+            ts = []
+            for _ in range(reps):
+                flush.fill_(1)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                ts.append((a, b))
+        torch.cuda.synchronize(device)
+        v = sorted(p.elapsed_time(q) for p, q in ts)
+        return v[len(v) // 2] / 1e3
+
+    sweep = {}
+    for t in (128, 256, 512, 8192):
+        xt = x[:t]
+        yt = y[:t]
+        tf = timed(lambda: ep.compressed_linear(db, xt, mode=ep.LINEAR_FUSED, out=yt, status=status, stream=stream))
+        ep.sync_status(status, stream)
+        yf = yt.float().cpu().numpy()
+        td = timed(lambda: ep.compressed_linear(db, xt, out=yt, workspace=ws, status=status, stream=stream))
+        tg = timed(lambda: ep.linear_bf16(xt, w_dense, out=yt, status=status, stream=stream))
+        tb = timed(lambda: torch.matmul(xt, w_dense.t()))
+        ep.sync_status(status, stream)
+        fl = 2.0 * t * N * K
+        r = np.unique(np.r_[0:2, t // 2, t - 1])
+        ref = (torch.from_numpy(synth.bf16_to_f32(x_bits[r])).double() @ w_hat.t()).numpy()
+        sweep[str(t)] = {"fused_us": tf * 1e6, "decode_then_gemm_us": td * 1e6, "dense_gemm_us": tg * 1e6,
+                         "cublas_dense_us": tb * 1e6, "fused_tflops": fl / tf / 1e12,
+                         "decode_then_gemm_tflops": fl / td / 1e12, "fused_passes": -(-t // ep.fused_tokens_per_pass(K)),
+                         "fused_max_rel_err_vs_fp64": float(np.abs(yf[r] - ref).max() / np.abs(ref).max())}
     return {"shape": "X 8192x3840 (N(0,1)) by W 10240x3840 (Student-t, 4.0 bpp)", "gflop": flops / 1e9,
             "compressed_linear_tflops": flops / t_cl / 1e12, "compressed_linear_ms": t_cl * 1e3,
             "compressed_linear_frac_of_peak": flops / t_cl / 1e12 / peak if peak else None,
             "mode": "decode into L2-resident workspace, then tcgen05 GEMM",
             "dense_tcgen05_tflops": flops / t_dense / 1e12, "dense_cublas_tflops": flops / t_torch / 1e12,
             "decode_ms": t_dec * 1e3, "overhead_pct_vs_dense_tcgen05": 100.0 * (t_cl / t_dense - 1.0),
-            "max_rel_err_vs_fp64": err, "err_rows": "12 sampled token rows", "peak_bf16_tflops": peak}
+            "max_rel_err_vs_fp64": err, "err_rows": "12 sampled token rows", "peak_bf16_tflops": peak,
+            "token_sweep": sweep,
+            "token_sweep_note": "L2 evicted before each call; fused = W decoded into shared memory as the tcgen05 "
+                                "B operand, no workspace"}
 
 
 def bench_comparators(ep, synth, torch, np, device, stream, peaks, copies: int = 16):

@@ -165,11 +165,11 @@ ep_status ep_allocate_bits(const ep_layer_ref *layers, int64_t n_layers, float a
 /* 8 * bytes / (rows * cols) after validating the stream ("actual_bpp", metadata included). */
 ep_status ep_actual_bpp(const uint8_t *blob, size_t bytes, double *bpp);
 /* Parse and fully validate a host copy of a stream and report its metadata
- * (shape, mode, container, resolution, sizes).  Serves the guide's advice,
- * when a restore fails, to compare the configuration and metadata on both
- * sides of the round trip and to check that the stored object carries all
- * that the decoder needs ("EntroPack PyTorch Guide", "Diagnose compression
- * failures in the correct order").  Errors: EP_ERR_INVALID_ARG (NULL),
+ * (shape, mode, container, resolution, sizes).  Serves the guide's advice
+ * for a failed restore: check that the settings and metadata agree before
+ * and after the round trip, and that the stored object holds everything the
+ * decoder reads ("EntroPack PyTorch Guide", "Diagnose compression failures
+ * in the correct order").  Errors: EP_ERR_INVALID_ARG (NULL),
  * EP_ERR_CORRUPT (any inconsistent header field, table, offset or size). */
 ep_status ep_query(const uint8_t *blob, size_t bytes, ep_info *out);
 
