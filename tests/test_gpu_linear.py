@@ -145,6 +145,27 @@ def test_fused_linear_matches_fp64(ep, T, N, K, with_bias):
     _check(y, x, oracle.container_to_f64(oracle.decode(blob)[0], "bf16"), bias_bits=b)
 
 
+def test_fused_linear_reports_corruption(ep):
+    # payload words changed on the device after the host validated the stream:
+    # the fused kernel's end-of-lane checks must flag it in the status word
+    w = synth.normal_bf16(68, 256, 512)
+    blob = oracle.encode(w, 4.0)
+    db = ep.DeviceBlob(blob)
+    h = oracle.header(blob)
+    b = bytearray(blob)
+    for off in range(h["payload_off"] + 200, h["payload_off"] + 2000, 97):
+        b[off] ^= 0xFF
+    db.device.copy_(torch.from_numpy(np.frombuffer(bytes(b), dtype=np.uint8).copy()).cuda())
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.compressed_linear(db, _bf16_dev(synth.normal_bf16(69, 64, 512, std=1.0)), mode=ep.LINEAR_FUSED, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & 0x1
+    db.device.copy_(db.host.cuda())  # the clean stream again: no flag
+    ep.compressed_linear(db, _bf16_dev(synth.normal_bf16(69, 64, 512, std=1.0)), mode=ep.LINEAR_FUSED, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+
+
 def test_fused_linear_unsupported_shapes(ep):
     assert ep.fused_tokens_per_pass(3840) == 640 and ep.fused_tokens_per_pass(200) == 0
     w = synth.normal_bf16(66, 64, 200)  # in_features not a multiple of 128
