@@ -374,29 +374,11 @@ __global__ void __launch_bounds__(1024, 1)
 }
 
 // ------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn fused_encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
 // X [T x K] row-major BF16 read in boxes of 128 tokens x 32 columns, which
 // land as 128 rows of 64 bytes, 64-byte swizzled (the swizzle span equals
 // the box row, so the rows are packed).  Tokens past T read as zero.
 bool make_x_map(CUtensorMap* map, const void* x, int64_t T, int64_t K) {
-    EncodeTiledFn fn = fused_encode_fn();
+    EncodeTiledFn fn = tensor_map_encoder();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)T};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};

@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "ep_format.hpp"
@@ -228,28 +229,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // ------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
 // Row-major bf16 matrix [outer x inner] read in boxes of [box_outer x 64] with
 // the 128-byte swizzle; out-of-range elements read as zero.
 bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
-    EncodeTiledFn fn = encode_fn();
+    EncodeTiledFn fn = tensor_map_encoder();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {inner * 2};
@@ -270,12 +253,16 @@ int sm_count() {
 
 ep_status gemm_launch(const uint16_t* d_x, const uint16_t* d_w, uint16_t* d_y, const uint16_t* d_bias, int64_t T,
                       int64_t N, int64_t K, uint32_t* d_status, cudaStream_t stream) {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
-    });
-    if (attr_err != cudaSuccess) return EP_ERR_CUDA;
+    // the shared-memory limit is a per-device setting: raise it once per device
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return EP_ERR_CUDA;
+    if (!(attr_done.load(std::memory_order_acquire) & (1ull << dev))) {
+        if (cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem) !=
+            cudaSuccess)
+            return EP_ERR_CUDA;
+        attr_done.fetch_or(1ull << dev, std::memory_order_release);
+    }
     CUtensorMap tx, tw;
     if (!make_map(&tx, d_x, (uint64_t)K, (uint64_t)T, BM) || !make_map(&tw, d_w, (uint64_t)K, (uint64_t)N, BN))
         return EP_ERR_CUDA;
@@ -305,6 +292,20 @@ ep_status check_gemm_args(const void* d_x, const void* d_w, const void* d_y, con
 }
 
 }  // namespace
+
+EncodeTiledFn tensor_map_encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
 
 // CompressedLinear on a stream already parsed and validated into L
 ep_status compressed_linear_parsed(const Layout& L, const void* d_blob, const uint16_t* d_x, int64_t tokens,

@@ -6,9 +6,19 @@
 // returns with an error flag instead of spinning forever.
 #pragma once
 
+#include <cuda.h>
+
 #include <cstdint>
 
 namespace ep {
+
+// cuTensorMapEncodeTiled, looked up once through the runtime's driver
+// entry-point query (NULL when the driver does not offer it).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
+
 namespace sm100 {
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
