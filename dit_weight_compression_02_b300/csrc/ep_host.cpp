@@ -1,8 +1,10 @@
 // Host-side stream parsing and validation, info queries and status strings.
 // A stream is validated completely before any kernel is launched, so that a
 // corrupt or truncated blob ends the call with a clear error instead of a
-// half-converted tensor ("EntroPack PyTorch Guide", "Fail cleanly" advice on
-// partial conversion; "Check metadata on both sides of the round trip").
+// half-converted tensor ("EntroPack PyTorch Guide", "Test saved artifacts and
+// reloads before deployment": a partial failure ends in a clear error;
+// "Diagnose compression failures in the correct order": the stored object must
+// hold everything the decoder reads).
 #include <cstdlib>
 #include <cstring>
 #include <new>
