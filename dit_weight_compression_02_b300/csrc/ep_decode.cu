@@ -18,6 +18,9 @@
 // (values beyond the direct byte range) are rare: the fast path is
 // branch-free and a warp-uniform test sends a block with any escape through
 // the slow path, which reads the escape payload's words from global memory.
+// A single lossy matrix with fewer tile groups than one wave of warps is bound
+// by one lane's chain of dependent symbols; it runs a software-pipelined block
+// loop (decode_group_pipelined) in 512-thread CTAs.
 //
 // Slot entry: f << 20 | u << 12 | (slot - cum_u), with f the 12-bit frequency
 // and u the symbol byte.  One LDS, one shift, one AND and one IMAD advance
@@ -237,6 +240,160 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
     }
 }
 
+// Latency-bound decode (a single matrix that fills fewer warps than the SMs
+// hold): the block loop is software pipelined so that one lane's work of two
+// neighbouring blocks overlaps.  While block j is checked for escapes,
+// rebuilt and stored, the symbols of block j + 1 are already decoded from the
+// state after block j's symbols, on the speculation that block j has no
+// escape.  A block with an escape (rare) restores the lane state saved before
+// the speculation, decodes its escape payload and decodes block j + 1 again.
+// Lossy streams only; the bits produced are those of decode_group.
+template <int KIND, bool DUMP, int NL, bool RAGGED>
+__device__ __forceinline__ void decode_group_pipelined(const DecodeArgs& a, const uint32_t* tab, int64_t grp0,
+                                                       uint32_t* status, uint32_t ring_off) {
+    void* const outp = a.out;
+    uint8_t* const symp = a.sym_out;
+    const int64_t cols = a.cols;
+    Lane ln[NL];
+    LaneTile<KIND> T[NL];
+    bool esc_bad[NL];
+#pragma unroll
+    for (int i = 0; i < NL; i++) {
+        T[i].setup(a, grp0 + i, ln[i], ring_off + kRingBytesPerLane * i, status);
+        esc_bad[i] = false;
+    }
+    // the 8 symbols of one block of every lane, as F = bits(1536 + u/2)
+    auto block_syms = [&](uint32_t (&D)[NL][8]) {
+        const uint32_t* t1[NL];
+#pragma unroll
+        for (int i = 0; i < NL; i++) {
+            D[i][0] = (ln[i].sym(tab) & 0x000FF000u) | kMagicLo;
+            t1[i] = tab + kSlots + ((D[i][0] >> 12) & 1u) * kSlots;  // context 1 + c
+        }
+#pragma unroll
+        for (int k = 1; k < 7; k++)
+#pragma unroll
+            for (int i = 0; i < NL; i++) D[i][k] = (ln[i].sym(t1[i]) & 0x000FF000u) | kMagicLo;
+#pragma unroll
+        for (int i = 0; i < NL; i++) D[i][7] = (ln[i].sym(t1[i] + 2 * kSlots) & 0x000FF000u) | kMagicLo;
+    };
+    uint32_t F[NL][8];
+    bool last_slow = false;
+    top_up<NL>(ln);
+    block_syms(F);
+#pragma unroll 2
+    for (int j = 0; j < kBlocksPerLane; j++) {
+        const int slab = j >> 5, row = j & 31;
+        float mult[NL];
+#pragma unroll
+        for (int i = 0; i < NL; i++)
+            mult[i] = __ldg((KIND == K_FP8 || KIND == K_INT8 ? T[i].mr : T[i].gr) + row);
+        // restore point: the lane state after block j's symbols
+        uint32_t sx[NL], sa[NL], sn[NL];
+#pragma unroll
+        for (int i = 0; i < NL; i++) {
+            sx[i] = ln[i].x;
+            sa[i] = ln[i].a;
+            sn[i] = ln[i].next;
+        }
+        const bool more = j + 1 < kBlocksPerLane;
+        uint32_t G[NL][8];
+        // unconditional, so that it shares a basic block with block j's
+        // reconstruction below; after the last block it decodes past the
+        // lane's end (ring reads only) and the state is restored after the loop
+        if ((j & 1) == 1) top_up<NL>(ln);  // block j + 1 starts a pair
+        block_syms(G);
+        bool esc[NL];
+        bool any = false;
+        float y[NL][8];
+#pragma unroll
+        for (int i = 0; i < NL; i++) {
+            bool v = ((F[i][0] >> 13) & 0x7Fu) == 0;  // s0 byte 0 or 1
+#pragma unroll
+            for (int k = 1; k < 8; k++) v |= (F[i][k] & 0x000FF000u) == 0;  // byte 0
+            esc[i] = v && T[i].active;
+            any |= esc[i];
+            // the fast path's values, computed before the vote so that they
+            // share a basic block with block j + 1's symbol chain
+            const uint32_t px = F[i][0] ^ F[i][1] ^ F[i][2] ^ F[i][3] ^ F[i][4] ^ F[i][5] ^ F[i][6];
+            const uint32_t f7 = F[i][7] + (px & 0x2000u);
+            const float cst = -mult[i] * kMagicLoQ;  // exact: mult has <= 7 significant bits
+#pragma unroll
+            for (int k = 0; k < 7; k++) y[i][k] = fmaf(__uint_as_float(F[i][k]), mult[i], cst);
+            y[i][7] = fmaf(__uint_as_float(f7), mult[i], cst);
+        }
+        if (__any_sync(0xffffffffu, any)) {
+            // rare: undo the speculation, decode block j's escape payloads (from
+            // global memory), then decode block j + 1 again from the new state
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+#pragma unroll
+            for (int i = 0; i < NL; i++) {
+                ln[i].x = sx[i];
+                ln[i].a = sa[i];
+                ln[i].next = sn[i];
+                const uint32_t c = (F[i][0] >> 12) & 1u;
+                int32_t B[8];
+#pragma unroll
+                for (int k = 0; k < 8; k++) B[k] = (int32_t)sym_byte(F[i][k]);
+                if (esc[i]) {
+#pragma unroll
+                    for (int k = 0; k < 8; k++) {
+                        const bool is_esc = (k == 0) ? (B[0] <= 1) : (B[k] == 0);
+                        if (!is_esc) continue;
+                        const uint32_t hi = ln[i].byte();
+                        const uint32_t lo = ln[i].byte();
+                        const int32_t P = (int32_t)(int16_t)(uint16_t)((hi << 8) | lo);
+                        const int32_t mask = (k == 7) ? 3 : 1;
+                        if (((P - (int32_t)c) & mask) != 0) esc_bad[i] = true;
+                        B[k] = P + 128;
+                    }
+                }
+                const int32_t px = B[0] ^ B[1] ^ B[2] ^ B[3] ^ B[4] ^ B[5] ^ B[6];
+                B[7] += px & 2;
+                const float cst = -mult[i] * kMagicHiQ;  // exact: mult has <= 7 significant bits
+#pragma unroll
+                for (int k = 0; k < 8; k++) y[i][k] = fmaf(__uint_as_float(kMagicHi + (uint32_t)B[k]), mult[i], cst);
+            }
+            if (more) {
+                top_up<NL>(ln);
+                block_syms(G);
+            } else {
+                last_slow = true;  // the state is the lane's true end state
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NL; i++) {
+            const bool st = T[i].active && (!RAGGED || (T[i].col0 + kSlabCols * slab < cols && row < T[i].rows_left));
+            if (st) {
+                const int64_t eoff = T[i].base + kSlabCols * slab + (int64_t)row * cols;
+                store_block<KIND>(outp, eoff, y[i]);
+                if (DUMP) {
+                    uint32_t u[8];
+#pragma unroll
+                    for (int k = 0; k < 8; k++) u[k] = sym_byte(F[i][k]);
+                    dump_syms(symp, eoff, u);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NL; i++)
+#pragma unroll
+            for (int k = 0; k < 8; k++) F[i][k] = G[i][k];
+        if (!more && !last_slow)
+#pragma unroll
+            for (int i = 0; i < NL; i++) {  // undo the decode past the lane's end
+                ln[i].x = sx[i];
+                ln[i].a = sa[i];
+                ln[i].next = sn[i];
+            }
+    }
+#pragma unroll
+    for (int i = 0; i < NL; i++) {
+        if (T[i].active && (ln[i].x != kRansL || ln[i].a != ln[i].aend)) flag(status, EP_STATUS_LANE_END);
+        if (esc_bad[i]) flag(status, EP_STATUS_ESCAPE);
+    }
+}
+
 __device__ __forceinline__ void copy_row_scales(const DecodeArgs& a, int64_t first, int64_t stride) {
     if (a.scale_out)
         for (int64_t r = first; r < a.rows; r += stride) a.scale_out[r] = a.t[r];
@@ -282,6 +439,25 @@ __global__ void __launch_bounds__(cta_threads(NL), 1) decode_kernel(const Decode
     const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 5);
     for (int64_t p = (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x; p < n_jobs; p += stride)
         decode_group<KIND, DUMP, NL, RAGGED>(a, tab, p * NL, a.status, lane_ring<NL>(a.n_ctx));
+}
+
+// Latency-bound single matrices (lossy): one lane per thread, 512 threads, the
+// pipelined block loop.
+constexpr int kPipeThreads = 512;
+
+template <int KIND, bool DUMP, bool RAGGED>
+__global__ void __launch_bounds__(kPipeThreads, 1) decode_kernel_pipe(const DecodeArgs a) {
+    uint32_t* const smem = g_smem;
+    uint32_t* tab = smem;
+    uint32_t* fr = smem + a.n_ctx * kSlots;
+    uint32_t* cu = fr + a.n_ctx * 256;
+    build_tables(a, tab, fr, cu);
+    if (KIND == K_FP8 || KIND == K_INT8)
+        copy_row_scales(a, (int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
+    const int64_t n_groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
+    const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t p = (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x; p < n_groups; p += stride)
+        decode_group_pipelined<KIND, DUMP, 1, RAGGED>(a, tab, p, a.status, lane_ring<1>(a.n_ctx));
 }
 
 // ----------------------------------------------------------------- batched
@@ -412,8 +588,23 @@ ep_status launch_nl(const DecodeArgs& a, cudaStream_t stream) {
 bool is_ragged(int64_t rows, int64_t cols) { return (rows % kTileRows) != 0 || (cols % kTileCols) != 0; }
 
 template <int KIND, bool DUMP, bool RAGGED>
+ep_status launch_pipe(const DecodeArgs& a, cudaStream_t stream) {
+    static std::atomic<uint64_t> done{0};
+    if (raise_smem_limit(reinterpret_cast<const void*>(decode_kernel_pipe<KIND, DUMP, RAGGED>), &done) != EP_OK)
+        return EP_ERR_CUDA;
+    const int64_t groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
+    const int64_t cap = device_info().sms;
+    const int grid = (int)(groups < cap ? groups : cap);
+    const size_t smem = (size_t)a.n_ctx * (kSlots + 512) * 4 + (size_t)kPipeThreads * kRingBytesPerLane;
+    decode_kernel_pipe<KIND, DUMP, RAGGED><<<grid, kPipeThreads, smem, stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+template <int KIND, bool DUMP, bool RAGGED>
 ep_status launch_r(const DecodeArgs& a, cudaStream_t stream) {
     const int64_t groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
+    if constexpr (!is_lossless(KIND))
+        if (groups <= (int64_t)device_info().sms * (kPipeThreads / 32)) return launch_pipe<KIND, DUMP, RAGGED>(a, stream);
     if (DUMP || groups <= (int64_t)device_info().sms * (kThreads / 32))
         return launch_nl<KIND, DUMP, 1, RAGGED>(a, stream);
     return launch_nl<KIND, DUMP, 2, RAGGED>(a, stream);

@@ -192,13 +192,16 @@ struct Lane {
     }
     // x < 2^16: shift in the prefetched word, then read the following one.  Only
     // lanes that refilled touch shared memory; the new word is first used one
-    // symbol later, by which time the load has landed.
+    // symbol later, by which time the load has landed.  Written without a
+    // branch (selects and a predicated load) so that the compiler can
+    // schedule the symbol chain together with independent work around it.
     __device__ __forceinline__ void renorm() {
-        if (x < kRansL) {
-            x = (x << 16) | next;
-            a += 2u;
-            next = word_at(a);
-        }
+        const uint32_t r = x < kRansL;
+        x = r ? ((x << 16) | next) : x;
+        a += r << 1;
+        const uint32_t addr = (uint32_t)__cvta_generic_to_shared(g_smem) + (roff | (a & (kRingBytesPerLane - 2u)));
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p ld.shared.u16 %0, [%1];\n\t}"
+                     : "+r"(next) : "r"(addr), "r"(r));
     }
     // one table symbol; returns the slot entry
     __device__ __forceinline__ uint32_t sym(const uint32_t* tab) {
