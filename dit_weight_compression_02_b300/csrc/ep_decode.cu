@@ -186,28 +186,7 @@ __device__ __forceinline__ void decode_group(const DecodeArgs& a, const uint32_t
             for (int i = 0; i < NL; i++) {
                 float y[8];
                 if (slow) {
-                    const uint32_t c = (e[i][0] >> 12) & 1u;
-                    int32_t B[8];
-#pragma unroll
-                    for (int k = 0; k < 8; k++) B[k] = (int32_t)sym_byte(e[i][k]);
-                    if (esc[i]) {
-#pragma unroll
-                        for (int k = 0; k < 8; k++) {
-                            const bool is_esc = (k == 0) ? (B[0] <= 1) : (B[k] == 0);
-                            if (!is_esc) continue;
-                            const uint32_t hi = ln[i].byte();
-                            const uint32_t lo = ln[i].byte();
-                            const int32_t P = (int32_t)(int16_t)(uint16_t)((hi << 8) | lo);
-                            const int32_t mask = (k == 7) ? 3 : 1;
-                            if (((P - (int32_t)c) & mask) != 0) esc_bad[i] = true;
-                            B[k] = P + 128;
-                        }
-                    }
-                    const int32_t px = B[0] ^ B[1] ^ B[2] ^ B[3] ^ B[4] ^ B[5] ^ B[6];
-                    B[7] += px & 2;
-                    const float cst = -mult[i] * kMagicHiQ;  // exact: mult has <= 7 significant bits
-#pragma unroll
-                    for (int k = 0; k < 8; k++) y[k] = fmaf(__uint_as_float(kMagicHi + (uint32_t)B[k]), mult[i], cst);
+                    escape_block(ln[i], e[i], esc[i], mult[i], y, esc_bad[i]);
                 } else {
                     uint32_t F[8];
 #pragma unroll
@@ -331,28 +310,7 @@ __device__ __forceinline__ void decode_group_pipelined(const DecodeArgs& a, cons
                 ln[i].x = sx[i];
                 ln[i].a = sa[i];
                 ln[i].next = sn[i];
-                const uint32_t c = (F[i][0] >> 12) & 1u;
-                int32_t B[8];
-#pragma unroll
-                for (int k = 0; k < 8; k++) B[k] = (int32_t)sym_byte(F[i][k]);
-                if (esc[i]) {
-#pragma unroll
-                    for (int k = 0; k < 8; k++) {
-                        const bool is_esc = (k == 0) ? (B[0] <= 1) : (B[k] == 0);
-                        if (!is_esc) continue;
-                        const uint32_t hi = ln[i].byte();
-                        const uint32_t lo = ln[i].byte();
-                        const int32_t P = (int32_t)(int16_t)(uint16_t)((hi << 8) | lo);
-                        const int32_t mask = (k == 7) ? 3 : 1;
-                        if (((P - (int32_t)c) & mask) != 0) esc_bad[i] = true;
-                        B[k] = P + 128;
-                    }
-                }
-                const int32_t px = B[0] ^ B[1] ^ B[2] ^ B[3] ^ B[4] ^ B[5] ^ B[6];
-                B[7] += px & 2;
-                const float cst = -mult[i] * kMagicHiQ;  // exact: mult has <= 7 significant bits
-#pragma unroll
-                for (int k = 0; k < 8; k++) y[i][k] = fmaf(__uint_as_float(kMagicHi + (uint32_t)B[k]), mult[i], cst);
+                escape_block(ln[i], F[i], esc[i], mult[i], y[i], esc_bad[i]);
             }
             if (more) {
                 top_up<NL>(ln);

@@ -256,6 +256,39 @@ __device__ __forceinline__ void flag(uint32_t* status, uint32_t bits) { atomicOr
 
 __device__ __forceinline__ uint32_t sym_byte(uint32_t e) { return (e >> 12) & 0xFFu; }
 
+// The escape path of one lane's block.  v[k] holds the coded byte of
+// coordinate k in bits 12..19 (a slot entry or a spliced float); when `esc`,
+// every escaped coordinate (s0 byte 0 or 1, s1..s7 byte 0) takes its int16
+// payload from the lane's words, two uniform bytes each.  Writes
+// y[k] = fp32(mult * q_k), rounded once (mult has at most 7 significant bits,
+// so mult * 6291520 is exact), and flags a payload that contradicts the
+// coset.
+__device__ __forceinline__ void escape_block(Lane& ln, const uint32_t* v, bool esc, float mult, float* y,
+                                             bool& esc_bad) {
+    const uint32_t c = (v[0] >> 12) & 1u;
+    int32_t B[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) B[k] = (int32_t)sym_byte(v[k]);
+    if (esc) {
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const bool is_esc = (k == 0) ? (B[0] <= 1) : (B[k] == 0);
+            if (!is_esc) continue;
+            const uint32_t hi = ln.byte();
+            const uint32_t lo = ln.byte();
+            const int32_t P = (int32_t)(int16_t)(uint16_t)((hi << 8) | lo);
+            const int32_t mask = (k == 7) ? 3 : 1;
+            if (((P - (int32_t)c) & mask) != 0) esc_bad = true;
+            B[k] = P + 128;
+        }
+    }
+    const int32_t px = B[0] ^ B[1] ^ B[2] ^ B[3] ^ B[4] ^ B[5] ^ B[6];
+    B[7] += px & 2;
+    const float cst = -mult * kMagicHiQ;
+#pragma unroll
+    for (int k = 0; k < 8; k++) y[k] = fmaf(__uint_as_float(kMagicHi + (uint32_t)B[k]), mult, cst);
+}
+
 __device__ __forceinline__ uint32_t pack2(float a, float b, int kind) {
     if (kind == K_BF16) {
         __nv_bfloat162 h = __floats2bfloat162_rn(a, b);

@@ -278,28 +278,7 @@ __global__ void __launch_bounds__(1024, 1)
                     float yv[8];
                     if (slow) {
                         asm volatile("cp.async.wait_group 0;" ::: "memory");
-                        const uint32_t c = (e[0] >> 12) & 1u;
-                        int32_t B[8];
-#pragma unroll
-                        for (int k = 0; k < 8; k++) B[k] = (int32_t)sym_byte(e[k]);
-                        if (esc) {
-#pragma unroll
-                            for (int k = 0; k < 8; k++) {
-                                const bool is_esc = (k == 0) ? (B[0] <= 1) : (B[k] == 0);
-                                if (!is_esc) continue;
-                                const uint32_t hi = ln[0].byte();
-                                const uint32_t lo = ln[0].byte();
-                                const int32_t P = (int32_t)(int16_t)(uint16_t)((hi << 8) | lo);
-                                const int32_t mask = (k == 7) ? 3 : 1;
-                                if (((P - (int32_t)c) & mask) != 0) esc_bad = true;
-                                B[k] = P + 128;
-                            }
-                        }
-                        const int32_t px = B[0] ^ B[1] ^ B[2] ^ B[3] ^ B[4] ^ B[5] ^ B[6];
-                        B[7] += px & 2;
-                        const float cst = -g * kMagicHiQ;
-#pragma unroll
-                        for (int k = 0; k < 8; k++) yv[k] = fmaf(__uint_as_float(kMagicHi + (uint32_t)B[k]), g, cst);
+                        escape_block(ln[0], e, esc, g, yv, esc_bad);
                     } else {
                         uint32_t F[8];
 #pragma unroll
