@@ -176,6 +176,29 @@ def test_escape_heavy(ep, container):
     _check(ep, blob)
 
 
+@pytest.mark.parametrize("container", ["bf16", "int8"])
+def test_escapes_in_every_lanes_last_block(ep, container):
+    # outliers in the last row of every tile's last K-slab: each lane's final
+    # block (step 127) escapes, so the latency-bound decode's speculative
+    # decode of the block after the last one is rolled back on the escape
+    # path, and the lane must still end exactly at its last word
+    w = synth.normal_bf16(17, 256, 1024)
+    f = synth.bf16_to_f32(w)
+    for q in range(4):  # the first coordinate of each lane's last block
+        f[31::32, 96 + 8 * q::128] = 2.0 if q % 2 else -2.0
+    w = (f.view(np.uint32) >> 16).astype(np.uint16)
+    blob = oracle.encode(w, 7.0, container)
+    sym = oracle.decode_symbols(blob)
+    for q in range(4):  # s0 escaped: its byte is the coset bit, 0 or 1
+        assert (sym[31::32, 96 + 8 * q::128] <= 1).all()
+    _check(ep, blob)
+    # the same stream through the batched kernel
+    db = ep.DeviceBlob(blob)
+    out = db.alloc_out()
+    ep.BatchDecoder([db], [out], ring=0)()
+    assert (_np(out) == oracle.decode(blob)[0]).all()
+
+
 def test_long_lanes_8bpp(ep):
     _check(ep, oracle.encode(synth.normal_bf16(13, 256, 1024), 8.0))
 
