@@ -310,6 +310,7 @@ def run_ours(args, rank, world, device):
         "configs": configs,
         "cpu_baseline": cpu,
         "setup_s": setup_s,
+        "library_encode_mparams_s": n_params / setup_s / 1e6,
         "wall_s_timed": wall,
         "kernel_source_sha": sha,
     }
@@ -635,7 +636,15 @@ def cpu_baseline(blobs, shapes, n_layers):
     for b in sample:
         oracle.decode_threaded(b, threads)
     dt = time.perf_counter() - t
+    # the oracle's encoder (one host thread) on the model's first layer
+    import synth
+    w0 = synth.student_t5_bf16(3, *shapes[0])
+    te = time.perf_counter()
+    oracle.encode(w0, 4.0)
+    te = time.perf_counter() - te
     return {"value": params / dt / 1e9, "unit": "G params/s", "cores": threads, "cpu_model": cpu_model(),
+            "oracle_encode": {"mparams_s": w0.size / te / 1e6, "seconds": te, "threads": 1,
+                              "sample": f"layer 0 ({shapes[0][0]}x{shapes[0][1]}) at 4.0 bpp"},
             "kind": "oracle",
             "sample": f"first {n_layers} layers ({params / 1e6:.0f} M params) of the same model, decoded to BF16 by "
                       f"the plain C oracle on {threads} host threads (contiguous tile ranges)",
