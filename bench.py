@@ -409,6 +409,8 @@ def bench_linear(ep, synth, torch, np, device, stream, peaks):
     return {"shape": "X 8192x3840 (N(0,1)) by W 10240x3840 (Student-t, 4.0 bpp)", "gflop": flops / 1e9,
             "compressed_linear_tflops": flops / t_cl / 1e12, "compressed_linear_ms": t_cl * 1e3,
             "compressed_linear_frac_of_peak": flops / t_cl / 1e12 / peak if peak else None,
+            "compressed_linear_frac_of_sustained_peak": (flops / t_cl / 1e12 / peaks["bf16_tflops_sustained"]
+                                                         if peaks.get("bf16_tflops_sustained") else None),
             "mode": "decode into L2-resident workspace, then tcgen05 GEMM",
             "dense_tcgen05_tflops": flops / t_dense / 1e12, "dense_cublas_tflops": flops / t_torch / 1e12,
             "decode_ms": t_dec * 1e3, "overhead_pct_vs_dense_tcgen05": 100.0 * (t_cl / t_dense - 1.0),
