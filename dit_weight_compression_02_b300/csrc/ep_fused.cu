@@ -77,7 +77,7 @@ struct FusedShape {
 struct FusedSmem {
     uint32_t rings, xs, wb, bars, total;
 };
-constexpr uint32_t kFusedBarBytes = 80;  // 8 mbarriers and the TMEM address
+constexpr uint32_t kFusedBarBytes = (2 * kXStages + 4) * 8 + 8;  // the mbarriers below and the TMEM address
 
 __host__ __device__ inline FusedSmem fused_smem(int n_ctx, int n_lanes, int R, int tc, uint32_t base_mod1024) {
     FusedSmem m;
