@@ -402,6 +402,10 @@ __global__ void __launch_bounds__(cta_threads(NL), 1) decode_kernel(const Decode
 // Latency-bound single matrices (lossy): one lane per thread, 512 threads, the
 // pipelined block loop.
 constexpr int kPipeThreads = 512;
+// The pipelined kernel pays off while the SMs hold few warps; from about nine
+// tile groups per SM on, the one-lane kernel's extra warps hide the latency as
+// well (8192 x 8192: 2048 groups, measured 3-4 % faster on the one-lane kernel)
+constexpr int kPipeGroupsPerSM = 9;
 
 template <int KIND, bool DUMP, bool RAGGED>
 __global__ void __launch_bounds__(kPipeThreads, 1) decode_kernel_pipe(const DecodeArgs a) {
@@ -562,7 +566,7 @@ template <int KIND, bool DUMP, bool RAGGED>
 ep_status launch_r(const DecodeArgs& a, cudaStream_t stream) {
     const int64_t groups = (a.n_tiles + kTilesPerWarp - 1) / kTilesPerWarp;
     if constexpr (!is_lossless(KIND))
-        if (groups <= (int64_t)device_info().sms * (kPipeThreads / 32)) return launch_pipe<KIND, DUMP, RAGGED>(a, stream);
+        if (groups <= (int64_t)device_info().sms * kPipeGroupsPerSM) return launch_pipe<KIND, DUMP, RAGGED>(a, stream);
     if (DUMP || groups <= (int64_t)device_info().sms * (kThreads / 32))
         return launch_nl<KIND, DUMP, 1, RAGGED>(a, stream);
     return launch_nl<KIND, DUMP, 2, RAGGED>(a, stream);
