@@ -145,6 +145,20 @@ def test_fused_linear_matches_fp64(ep, T, N, K, with_bias):
     _check(y, x, oracle.container_to_f64(oracle.decode(blob)[0], "bf16"), bias_bits=b)
 
 
+@pytest.mark.parametrize("T,N,K", [(100, 15360, 128), (300, 15360, 256)])
+def test_fused_linear_several_units_per_cta(ep, T, N, K):
+    # more units (three tile rows each) than SMs: CTAs take a second unit, so
+    # the accumulators are read back and reused, and the half-slab barriers
+    # carry on across units
+    w = synth.student_t5_bf16(N + 7 * K, N, K)
+    x = synth.normal_bf16(T + 11 * K, T, K, std=1.0)
+    blob = oracle.encode(w, 4.0)
+    n_units = -(-(N // 32) // 3)
+    assert n_units > torch.cuda.get_device_properties(0).multi_processor_count
+    y = ep.compressed_linear(ep.DeviceBlob(blob), _bf16_dev(x), mode=ep.LINEAR_FUSED)
+    _check(y, x, oracle.container_to_f64(oracle.decode(blob)[0], "bf16"))
+
+
 def test_fused_linear_reports_corruption(ep):
     # payload words changed on the device after the host validated the stream:
     # the fused kernel's end-of-lane checks must flag it in the status word
